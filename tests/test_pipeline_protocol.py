@@ -1,0 +1,147 @@
+"""Host simulation of the warp-role pipeline protocol (no GPU).
+
+The kernel's roles talk only through mbarriers:
+* operand ring: the producer waits ``consumed[s]`` with parity ``((phase // S) & 1) ^ 1``,
+  fills slot ``s = phase % S`` and completes ``loaded[s]``; the MMA role waits
+  ``loaded[s]`` with parity ``(phase // S) & 1``, reads slot ``s`` and completes
+  ``consumed[s]``, with ``phase = w * k_blocks + k`` on both sides
+  ("[Feature] Introduce tile scheduler #2441", gemm_tcgen5mma_ws_persistent.py,
+  ``gemm_persistent`` TMA and MMA loops; the review comment on that file asks for
+  ``phase % num_stages`` in the consumer too, which this model uses);
+* accumulator double buffer: the MMA role waits ``tmem_empty[w & 1]`` with parity
+  ``((w // 2) & 1) ^ 1`` and completes ``tmem_full[w & 1]``; the epilogue waits
+  ``tmem_full[w & 1]`` with parity ``(w // 2) & 1`` and completes ``tmem_empty[w & 1]``.
+
+An mbarrier is modelled by its phase counter: a wait on parity ``P`` passes when the
+phase with that parity has completed, i.e. when ``P != phase_count & 1``.  The roles are
+interleaved at random; the model checks that every read sees the data written for the
+same (w, k), that no slot is refilled before it was read, and that nothing deadlocks.
+"""
+
+import random
+
+import pytest
+
+
+class Barrier:
+    def __init__(self):
+        self.phase = 0
+
+    def passes(self, parity):
+        return parity != (self.phase & 1)
+
+    def complete(self):
+        self.phase += 1
+
+
+def slot_of(phase, S):
+    return phase % S
+
+
+def parity_of(phase, S):
+    return (phase // S) & 1
+
+
+def run_ring(S, k_blocks, waves, seed, consumer_slot=None):
+    """Returns None if the protocol held, else a string naming the violation."""
+    rng = random.Random(seed)
+    loaded = [Barrier() for _ in range(S)]
+    consumed = [Barrier() for _ in range(S)]
+    data = [None] * S
+    unread = [False] * S
+    total = waves * k_blocks
+    prod = 0
+    cons = 0
+    cslot = consumer_slot or (lambda w, k, phase: slot_of(phase, S))
+    while cons < total:
+        moves = []
+        if prod < total and consumed[slot_of(prod, S)].passes(parity_of(prod, S) ^ 1):
+            moves.append("p")
+        if cons < total:
+            w, k = divmod(cons, k_blocks)
+            s = cslot(w, k, cons)
+            if loaded[s].passes(parity_of(cons, S)):
+                moves.append("c")
+        if not moves:
+            return f"deadlock at producer {prod}, consumer {cons}"
+        if rng.choice(moves) == "p":
+            s = slot_of(prod, S)
+            if unread[s]:
+                return f"slot {s} refilled before it was read (phase {prod})"
+            data[s] = prod
+            unread[s] = True
+            loaded[s].complete()
+            prod += 1
+        else:
+            w, k = divmod(cons, k_blocks)
+            s = cslot(w, k, cons)
+            if data[s] != cons:
+                return f"phase {cons} read the data of phase {data[s]}"
+            unread[s] = False
+            consumed[s].complete()
+            cons += 1
+    return None
+
+
+def run_accumulators(waves, seed):
+    rng = random.Random(seed)
+    full = [Barrier(), Barrier()]
+    empty = [Barrier(), Barrier()]
+    acc = [None, None]
+    mma = 0
+    epi = 0
+    while epi < waves:
+        moves = []
+        if mma < waves and empty[mma & 1].passes(((mma // 2) & 1) ^ 1):
+            moves.append("m")
+        if epi < waves and full[epi & 1].passes((epi // 2) & 1):
+            moves.append("e")
+        if not moves:
+            return f"deadlock at mma {mma}, epilogue {epi}"
+        if rng.choice(moves) == "m":
+            if acc[mma & 1] is not None:
+                return f"accumulator {mma & 1} overwritten before it was drained (w={mma})"
+            acc[mma & 1] = mma
+            full[mma & 1].complete()
+            mma += 1
+        else:
+            if acc[epi & 1] != epi:
+                return f"w={epi} drained the accumulator of w={acc[epi & 1]}"
+            acc[epi & 1] = None
+            empty[epi & 1].complete()
+            epi += 1
+    return None
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("k_blocks", [1, 2, 3, 4, 7, 32])
+def test_ring_protocol_holds(S, k_blocks):
+    for seed in range(40):
+        assert run_ring(S, k_blocks, waves=5, seed=seed) is None
+
+
+@pytest.mark.parametrize("waves", [1, 2, 3, 4, 9])
+def test_accumulator_double_buffer_holds(waves):
+    for seed in range(60):
+        assert run_accumulators(waves, seed) is None
+
+
+def test_consumer_indexing_slots_by_k_is_caught():
+    # the slot function flagged in review: consumer reads k % S while the producer
+    # writes phase % S; wrong whenever k_blocks % S != 0 and a CTA runs >= 2 tiles
+    S, k_blocks = 4, 3
+    bad = lambda w, k, phase: k % S
+    failures = [run_ring(S, k_blocks, waves=3, seed=s, consumer_slot=bad) for s in range(20)]
+    assert all(f is not None for f in failures)
+    # ...and invisible when k_blocks is a multiple of S (why it went unnoticed)
+    assert all(run_ring(4, 8, 3, s, consumer_slot=bad) is None for s in range(20))
+
+
+def test_parities_match_the_generated_sm90_pipeline():
+    # "tilelang" (generated kernel source of the 3-stage sm_90 GEMM): the consumer waits
+    # barrier k % 3 with parity (k % 6) / 3 and the producer waits barrier k % 3 + 3 with
+    # parity ((k % 6) / 3) ^ 1 -- the same functions as phase % S and (phase // S) & 1
+    for k in range(1000):
+        assert slot_of(k, 3) == k % 3
+        assert parity_of(k, 3) == (k % 6) // 3
+        assert parity_of(k, 3) ^ 1 == ((k % 6) // 3) ^ 1
