@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Throughput of the persistent warp-specialized GEMM on GB300: one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tg|reference]
+                    [--workload gemm_8192_bf16]
+
+A step is one pass of the whole hot path: one tg_gemm_persistent call (one kernel launch)
+on the workload's seeded synthetic inputs, already resident in HBM.  ``value`` is
+2MNK / (device time per step) in TFLOP/s, timed with CUDA events on the launching stream
+over K back-to-back steps after W warm-up steps.  The 8192^3 bf16 inputs (A + B = 256 MiB)
+are larger than the 129 MB L2, so no flush runs between steps.
+
+Also reported: ``e2e`` (the same metric through tg_gemm_persistent_host: pinned host A, B
+copied in and C copied out every step), ``roofline`` (tensor-bound: achieved TFLOP/s over
+the measured cuBLAS bf16 peak of this GPU type), ``clocks`` (nvidia-smi sampled during the
+timed region) and ``cpu_baseline`` (the CPU oracle timed on a bounded row slab of the same
+workload, which also checks the GPU's rows of that slab).
+
+``--impl reference`` times the CPU oracle instead (there is no other implementation of this
+path to run); under torchrun only rank 0 runs it.
+
+With N > 1 ranks (torchrun), every rank runs the whole workload on its own GPU (replicas:
+the path needs no exchange between GPUs); time is the max over ranks, value the sum.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) at 4096³/8192³ bf16 on 1 GB300; % of dense tensor peak"
+UNIT = "TFLOP/s"
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0       # GB300 dense bf16/fp16, no sparsity
+DENSE_FLOP_PER_CLK_PER_SM = 8192         # derived: one 128x256x16 MMA per 128 cycles
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_persistent_ws_8192_bf16.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
+    ap.add_argument("--workload", default="gemm_8192_bf16")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x, device=None):
+    """Max of a float over all ranks (the value itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def blas_threads():
+    """Threads numpy's BLAS uses (the oracle's matrix product), best effort."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    import ctypes
+
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({l.split()[-1] for l in f if "openblas" in l.lower() and ".so" in l})
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                        "openblas_get_num_threads"):
+                if hasattr(lib, sym):
+                    return int(getattr(lib, sym)())
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in a child process."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        lines = self.out.read().strip().splitlines()
+        self.out.close()
+        os.unlink(self.out.name)
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def profile_traffic():
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, or None if
+    the kernel sources changed since that capture."""
+    from persistent_warp_specialized_gb300 import _build
+
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("-* ")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("`")] = v.strip().strip("`")
+    if vals.get("source_stamp") != _build._stamp():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def oracle_slab(a_bits, b_bits, fmt, rows):
+    from oracle import gemm as ogemm
+
+    return ogemm.gemm_ref(a_bits[:rows], b_bits, fmt)
+
+
+def calibrate_rows(a_bits, b_bits, fmt, seconds):
+    """Rows of C the oracle computes in about ``seconds`` (at least 8)."""
+    M = a_bits.shape[0]
+    probe = min(M, 32)
+    t0 = time.perf_counter()
+    oracle_slab(a_bits, b_bits, fmt, probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    return int(max(min(M, probe * seconds / dt), min(M, 8)))
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    a, b = wl.workload_inputs(w)
+    a_bits, b_bits = wl.bits(a), wl.bits(b)
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    per_step = max(0.05, min(2.0, 150.0 / (steps + warm)))
+    rows = calibrate_rows(a_bits, b_bits, w.dtype, per_step)
+    for _ in range(warm):
+        oracle_slab(a_bits, b_bits, w.dtype, rows)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_slab(a_bits, b_bits, w.dtype, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * steps
+    value = flops / dt / 1e12
+    sample = (f"rows [0, {rows}) of C = A.B for {w.name} ({rows} x {w.N} outputs, K={w.K}) per step: "
+              f"decode, binary64 product, round to {w.dtype}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_out_dtype": w.dtype,
+            "accumulate": "fp32", "inputs": f"{w.dist}, seed {w.seed}",
+            "l2": "inputs larger than L2 (no flush)" if 2 * (w.M * w.K + w.K * w.N) > 129e6
+                  else "inputs fit in L2 (no flush; warm L2)",
+            "tile": "128x256x64, 4 stages, persistent grid = #SMs"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_tg(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist(world, "nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import persistent_warp_specialized_gb300 as tg
+    from persistent_warp_specialized_gb300 import _build
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    _build.build()
+    tg.load_library()
+    w = wl.WORKLOADS[args.workload]
+    a_cpu, b_cpu = wl.workload_inputs(w)
+    a = a_cpu.to(dev)
+    b = b_cpu.to(dev)
+    c = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.dtype], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def step():
+        tg.tg_gemm_persistent(a, b, c, w.M, w.N, w.K, w.dtype, stream)
+
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize(dev)
+    tg.tg_device_status(stream)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    ms_local = ev0.elapsed_time(ev1) / steps
+    tg.tg_device_status(stream)
+    ms = max_over_ranks(ms_local, dev if world > 1 else None)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point: H2D A, B + kernel + D2H C per step
+    a_h, b_h = a_cpu.pin_memory(), b_cpu.pin_memory()
+    c_h = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.dtype]).pin_memory()
+    a2, b2, c2 = torch.empty_like(a), torch.empty_like(b), torch.empty_like(c)
+
+    def e2e_step():
+        tg.tg_gemm_persistent_host(a_h, b_h, c_h, a2, b2, c2, w.M, w.N, w.K, w.dtype, stream)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(1, args.e2e_steps)
+    barrier()
+    ev0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e_steps, dev if world > 1 else None)
+    tg.tg_device_status(stream)
+    h2d = 2 * (w.M * w.K + w.K * w.N)
+    d2h = 2 * w.M * w.N
+    e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    peaks, peak_src = measured_peaks()
+    achieved = w.flops / (ms_local * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if w.dtype == "f16":
+        peak_note = "bf16 peak x 1 (fp16 and bf16 share the dense tensor rate)"
+    else:
+        peak_note = "bf16 burst peak"
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": profile_traffic(),
+                "peak_source": f"{peak_src} ({peak_note}, cuBLAS torch.matmul)",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "frac_of_nominal_dense": achieved / NOMINAL_DENSE_BF16_TFLOPS,
+                "nominal_dense_tflops": NOMINAL_DENSE_BF16_TFLOPS}
+    if clocks and clocks.get("sm_mhz"):
+        clk_peak = sms * DENSE_FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12
+        roofline["frac_of_clock_peak"] = achieved / clk_peak
+        roofline["clock_peak_tflops"] = clk_peak
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see config.inputs)",
+        "config": dict(workload_config(w), sms=sms, grid=min(sms, -(-w.M // 128) * -(-w.N // 256))),
+        "gpu_launches": steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+
+        from oracle import formats
+
+        a_bits, b_bits = wl.bits(a_cpu), wl.bits(b_cpu)
+        rows = calibrate_rows(a_bits, b_bits, w.dtype, args.cpu_seconds)
+        t_0 = time.perf_counter()
+        ref = oracle_slab(a_bits, b_bits, w.dtype, rows)
+        dt = time.perf_counter() - t_0
+        got = formats.decode(wl.bits(c[:rows].cpu()), w.dtype)
+        want = formats.decode(ref, w.dtype)
+        err = np.abs(got - want)
+        ok = bool(np.isfinite(got).all() and (err <= 5e-3 + 1e-2 * np.abs(want)).all())
+        line["cpu_baseline"] = {
+            "value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"rows [0, {rows}) of C ({rows} x {w.N} outputs, K={w.K}): decode, "
+                      f"binary64 product (numpy/OpenBLAS), round to {w.dtype}; {dt:.1f} s"}
+        line["parity_sample"] = {"rows": rows, "cols": w.N, "within_tolerance": ok,
+                                 "max_abs_err": float(err.max())}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_tg(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,124 @@
+/*
+ * tg.h -- C ABI of the persistent, warp-specialized GEMM for GB300 (sm_103a).
+ *
+ *   C[M, N] = A[M, K] . B[K, N]      fp16 or bf16 in, fp32 accumulation, same type out
+ *
+ * The operation is the one ``gemm_persistent`` computes in "[Feature] Introduce tile
+ * scheduler #2441" (examples/gemm_sm100/gemm_tcgen5mma_ws_persistent.py): row-major
+ * A [M, K] and B [K, N] (``T.tcgen05_gemm(A_shared, B_shared, ...)`` with neither operand
+ * transposed), fp32 accumulation in tensor memory, and a cast of the accumulator to the
+ * output type in the epilogue.  The call convention -- plain pointers, an int status,
+ * a readable last-error string -- follows the host wrapper that TileLang generates
+ * ("tilelang", Generated Kernel Source: ``init()``, ``call(A, B, C, stream)`` returning
+ * 0 or -1, ``get_last_error()``), and the argument checks follow the host checks of its
+ * lowered host module ("tilelang", 1.2 Pass Pipeline, Host IRModule: null data pointers,
+ * rank-2 row-major with unit inner stride and no byte offset, "vectorize dimension
+ * divisible by 8").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers of the current CUDA device, allocated by the
+ *     caller (cudaMalloc or any allocator built on it); the library never frees them and
+ *     keeps no pointer after the call returns.  Matrices are dense row-major with no
+ *     padding: the row stride of A is K elements, of B and C it is N elements.
+ *   - ``stream`` is a cudaStream_t (NULL = the legacy default stream).  GEMM entry points
+ *     are asynchronous: TG_OK means the work was enqueued; faults during execution surface
+ *     at the caller's next synchronisation, as with any CUDA launch.
+ *   - A negative return is an error; tg_last_error() then holds a message (thread-local;
+ *     valid until the next call on the same thread).  On error nothing was enqueued.
+ */
+#ifndef TG_H
+#define TG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types: input, output and (internally) fp32 accumulation */
+enum { TG_F16 = 0, TG_BF16 = 1 };
+
+/* status codes */
+enum {
+  TG_OK = 0,
+  TG_ERR_ARG = -1,     /* null/non-device pointer, negative size, unknown dtype, C overlapping A or B */
+  TG_ERR_ALIGN = -2,   /* pointer not 16-byte aligned, or N or K not a multiple of 8 (TMA row strides
+                          must be multiples of 16 bytes) */
+  TG_ERR_CUDA = -3,    /* a CUDA runtime/driver call failed, or the device is not sm_103 */
+  TG_ERR_TIMEOUT = -4  /* a bounded wait inside the kernel gave up (watchdog); see tg_device_status */
+};
+
+/*
+ * tg_gemm_persistent -- C = A . B on ``stream``.
+ *   A_dev [M, K], B_dev [K, N], C_dev [M, N]; all of type ``dtype`` (TG_F16 or TG_BF16).
+ *   M, N, K >= 0 and < 2^31.  N % 8 == 0 and K % 8 == 0.  All three pointers 16-byte aligned.
+ *   C must not overlap A or B.  M == 0 or N == 0: nothing is done.  K == 0: C is zero-filled.
+ * One persistent CTA per SM (at most the number of output tiles) walks 128 x 256 output tiles
+ * in grouped order (group 8); see tg_tile_schedule.  Partial edge tiles in M and N and a
+ * partial last k-block are handled inside the kernel (zero-filled loads, clipped stores).
+ */
+int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
+                       int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
+/*
+ * tg_tile_schedule -- the tile order the GEMM kernel follows, for inspection.
+ * The persistent scheduler of "[Feature] Introduce tile scheduler #2441"
+ * (``PersistentTileScheduler(..., swizzle_size=group_size)``, ``init(block_id)``,
+ * ``valid()``, ``next_tile()``) runs on the device, one thread per worker, with the same
+ * scheduler code the GEMM kernel's three roles use.
+ *   m_blocks, n_blocks >= 1 with m_blocks * n_blocks < 2^31; num_sms >= 1 (workers); group >= 1.
+ *   out_host: HOST buffer of 4 * m_blocks * n_blocks int32, filled with rows
+ *   (worker, w, bx, by) ordered by worker, then by the worker's iteration clock w;
+ *   bx is the M-tile, by the N-tile.
+ * Synchronous (uses and synchronises the legacy default stream; allocates and frees a
+ * temporary device buffer).  Returns the row count (= m_blocks * n_blocks) or an error.
+ */
+int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* tg_last_error(void);
+
+/*
+ * tg_gemm_config -- the compile-time tiling, for callers that size schedules or buffers.
+ * Any pointer may be NULL.  Returns TG_OK.
+ */
+int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* group);
+
+/*
+ * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
+ *   trace_dev: NULL or a device buffer of 4 * m_blocks * n_blocks int32; row t (t = the
+ *     linear tile id) receives (cta, w, bx, by) as the epilogue of the CTA that stored tile t
+ *     saw them -- evidence that the kernel followed the schedule of tg_tile_schedule.
+ *   watchdog_ns: limit for every wait inside the kernel (0 = the default of about 4 s).
+ *   inject_skip_phase: -1 for none; otherwise CTA 0's producer never fills that pipeline
+ *     phase, so the MMA role's wait on it cannot complete: the watchdog must fire, every
+ *     role must stop, and the call must return TG_ERR_TIMEOUT with the context intact.
+ * Synchronises ``stream``.  Returns TG_OK, TG_ERR_TIMEOUT or another error.
+ */
+int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev,
+                             int64_t M, int64_t N, int64_t K, int dtype, void* stream,
+                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase);
+
+/*
+ * tg_device_status -- synchronises ``stream``, then reads and clears the current device's
+ * watchdog word.  TG_OK if no kernel launched by this library on the device gave up a wait
+ * since the last call; TG_ERR_TIMEOUT otherwise (its output must not be trusted).
+ */
+int tg_device_status(void* stream);
+
+/*
+ * tg_gemm_persistent_host -- end-to-end form for data that lives in host memory.
+ *   A_host [M, K], B_host [K, N] are copied to the caller's device buffers A_dev, B_dev, the
+ *   GEMM runs into C_dev, and C_dev is copied back to C_host, all enqueued on ``stream`` in
+ *   that order.  Host buffers should be page-locked (cudaHostAlloc) for the copies to be
+ *   asynchronous.  Same size, type and alignment rules as tg_gemm_persistent.
+ */
+int tg_gemm_persistent_host(const void* A_host, const void* B_host, void* C_host,
+                            void* A_dev, void* B_dev, void* C_dev,
+                            int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_H */

@@ -1,0 +1,168 @@
+"""Python binding of libtg, the persistent warp-specialized GEMM for GB300 (sm_103a).
+
+Argument marshalling only: every function here forwards to the C entry point of the same
+name declared in ``include/tg.h``; all of the GEMM and the tile scheduling run in the
+library's CUDA kernels.  Tensors are passed by their device pointers (``data_ptr()``);
+PyTorch only provides device memory and streams.  There is no fallback: if ``libtg.so``
+is missing or fails to load, every call raises.
+
+Build the library with ``persistent_warp_specialized_gb300._build.build()`` (nvcc, sm_103a).
+"""
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtg.so")
+
+TG_F16 = 0
+TG_BF16 = 1
+TG_OK = 0
+TG_ERR_ARG = -1
+TG_ERR_ALIGN = -2
+TG_ERR_CUDA = -3
+TG_ERR_TIMEOUT = -4
+
+DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
+
+EXPORTED = (
+    "tg_gemm_persistent",
+    "tg_tile_schedule",
+    "tg_last_error",
+    "tg_gemm_config",
+    "tg_gemm_persistent_debug",
+    "tg_device_status",
+    "tg_gemm_persistent_host",
+)
+
+
+class TgError(RuntimeError):
+    def __init__(self, code, message):
+        super().__init__(f"tg error {code}: {message}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path=LIB_PATH):
+    """Load libtg.so (once) and declare its C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is not built; run persistent_warp_specialized_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+    lib.tg_gemm_persistent.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.tg_gemm_persistent.restype = i32
+    lib.tg_tile_schedule.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.tg_tile_schedule.restype = i32
+    lib.tg_last_error.argtypes = []
+    lib.tg_last_error.restype = ctypes.c_char_p
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
+    lib.tg_gemm_config.restype = i32
+    lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, u64, i64]
+    lib.tg_gemm_persistent_debug.restype = i32
+    lib.tg_device_status.argtypes = [vp]
+    lib.tg_device_status.restype = i32
+    lib.tg_gemm_persistent_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.tg_gemm_persistent_host.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc < 0:
+        raise TgError(rc, load_library().tg_last_error().decode(errors="replace"))
+    return rc
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):          # numpy array (host memory)
+        return x.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(x).__name__}")
+
+
+def _dtype(d):
+    return DTYPES[d] if isinstance(d, str) else int(d)
+
+
+def _stream(s):
+    if s is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def tg_last_error():
+    return load_library().tg_last_error().decode(errors="replace")
+
+
+def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
+    """C = A . B (device buffers; asynchronous on ``stream``, default: torch's current)."""
+    return _check(load_library().tg_gemm_persistent(
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
+
+
+def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, trace=None, watchdog_ns=0,
+                             inject_skip_phase=-1):
+    return _check(load_library().tg_gemm_persistent_debug(
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _ptr(trace),
+        watchdog_ns, inject_skip_phase))
+
+
+def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,
+                            stream=None):
+    return _check(load_library().tg_gemm_persistent_host(
+        _ptr(A_host), _ptr(B_host), _ptr(C_host), _ptr(A_dev), _ptr(B_dev), _ptr(C_dev),
+        M, N, K, _dtype(dtype), _stream(stream)))
+
+
+def tg_device_status(stream=None):
+    return _check(load_library().tg_device_status(_stream(stream)))
+
+
+def tg_gemm_config():
+    vals = [ctypes.c_int() for _ in range(5)]
+    _check(load_library().tg_gemm_config(*[ctypes.byref(v) for v in vals]))
+    keys = ("block_m", "block_n", "block_k", "stages", "group")
+    return dict(zip(keys, (v.value for v in vals)))
+
+
+def tg_tile_schedule(m_blocks, n_blocks, num_sms, group):
+    """Rows (worker, w, bx, by) of the device scheduler, as a list of 4-tuples."""
+    rows = max(0, m_blocks) * max(0, n_blocks)
+    buf = (ctypes.c_int32 * (4 * max(rows, 1)))()
+    n = _check(load_library().tg_tile_schedule(m_blocks, n_blocks, num_sms, group, buf))
+    return [tuple(buf[4 * i: 4 * i + 4]) for i in range(n)]
+
+
+def gemm(a, b, out=None, stream=None):
+    """torch convenience: C = a @ b for contiguous 2-D fp16/bf16 CUDA tensors."""
+    import torch
+
+    names = {torch.float16: "f16", torch.bfloat16: "bf16"}
+    if a.dtype != b.dtype or a.dtype not in names:
+        raise TypeError("a and b must both be float16 or both bfloat16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shapes {tuple(a.shape)} and {tuple(b.shape)} do not contract")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous row-major")
+    M, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=a.dtype, device=a.device)
+    tg_gemm_persistent(a, b, out, M, N, K, names[a.dtype], stream)
+    return out

@@ -1,0 +1,294 @@
+// tg_api.cu -- the C ABI declared in include/tg.h: argument checks, TMA descriptor
+// encoding, persistent grid sizing and launch.
+//
+// The checks follow the host-side asserts TileLang emits before a launch ("tilelang",
+// 1.2 Pass Pipeline, Host IRModule: non-null data, rank-2 row-major with unit inner
+// stride and zero byte offset, inner dimension divisible by 8), and the descriptor set-up
+// follows its generated ``call()`` ("tilelang", Generated Kernel Source:
+// cuTensorMapEncodeTiled per operand, error text kept for get_last_error()).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/tg.h"
+#include "tg_config.h"
+#include "tg_internal.h"
+
+namespace {
+
+thread_local char g_err[1024] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int fail_cuda(const char* what, cudaError_t e) {
+  return fail(TG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Per-device facts, established once per device: SM count, arch, kernel attributes.
+struct DeviceInfo {
+  int state = 0;  // 0 unknown, 1 ready, -1 unsupported
+  int sms = 0;
+  char why[256] = "";
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_ready(int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_CUDA, "device ordinal %d unsupported", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda("cudaDeviceGetAttribute", e);
+    if (major != 10 || minor != 3) {
+      d.state = -1;
+      snprintf(d.why, sizeof(d.why), "device %d is sm_%d%d; this library is built for sm_103a",
+               dev, major, minor);
+    } else if ((e = tg::prepare_gemm_kernels()) != cudaSuccess) {
+      return fail_cuda("cudaFuncSetAttribute(MaxDynamicSharedMemorySize)", e);
+    } else {
+      d.state = 1;
+      d.sms = sms;
+    }
+  }
+  if (d.state < 0) return fail(TG_ERR_CUDA, "%s", d.why);
+  if (sms_out) *sms_out = d.sms;
+  return TG_OK;
+}
+
+// The pointer must be device memory of the current device (TMA reads it directly).
+int check_device_ptr(const void* p, const char* name) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TG_ERR_ARG, "%s: not a CUDA pointer (%s)", name, cudaGetErrorString(e));
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (a.type != cudaMemoryTypeDevice || a.device != dev)
+    return fail(TG_ERR_ARG, "%s: must be device memory of the current device %d", name, dev);
+  return TG_OK;
+}
+
+bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer, const char* name) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * tg::kElemBytes};  // bytes between rows
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return TG_OK;
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Shared validation of the GEMM entry points.  *nothing_to_do is set for M == 0 or N == 0.
+int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
+             bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (dtype != TG_F16 && dtype != TG_BF16) return fail(TG_ERR_ARG, "unknown dtype %d", dtype);
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(TG_ERR_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                (long long)N, (long long)K);
+  if (M == 0 || N == 0) {
+    *nothing_to_do = true;
+    return TG_OK;
+  }
+  if (!C || (K > 0 && (!A || !B))) return fail(TG_ERR_ARG, "null matrix pointer");
+  if (N % 8 != 0 || K % 8 != 0)
+    return fail(TG_ERR_ALIGN, "N=%lld and K=%lld must be multiples of 8 (16-byte row strides)",
+                (long long)N, (long long)K);
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) ||
+      (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u))))
+    return fail(TG_ERR_ALIGN, "A, B and C must be 16-byte aligned");
+  const uint64_t m_blocks = (M + tg::kBM - 1) / tg::kBM, n_blocks = (N + tg::kBN - 1) / tg::kBN;
+  if (m_blocks * n_blocks > static_cast<uint64_t>(kMaxDim))
+    return fail(TG_ERR_ARG, "too many output tiles");
+  int rc;
+  if ((rc = check_device_ptr(C, "C")) != TG_OK) return rc;
+  if (K > 0) {
+    if ((rc = check_device_ptr(A, "A")) != TG_OK) return rc;
+    if ((rc = check_device_ptr(B, "B")) != TG_OK) return rc;
+    const uint64_t cb = uint64_t(M) * N * tg::kElemBytes;
+    if (overlaps(C, cb, A, uint64_t(M) * K * tg::kElemBytes) ||
+        overlaps(C, cb, B, uint64_t(K) * N * tg::kElemBytes))
+      return fail(TG_ERR_ARG, "C overlaps A or B");
+  }
+  return TG_OK;
+}
+
+int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
+              void* stream, bool debug, int32_t* trace, uint64_t watchdog_ns, int64_t inject) {
+  bool nothing = false;
+  int rc = validate(A, B, C, M, N, K, dtype, &nothing);
+  if (rc != TG_OK || nothing) return rc;
+  int sms = 0;
+  if ((rc = device_ready(&sms)) != TG_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = tg::launch_zero_fill(C, uint64_t(M) * N * tg::kElemBytes, s);
+    return e == cudaSuccess ? TG_OK : fail_cuda("zero fill launch", e);
+  }
+  tg::GemmLaunch l;
+  if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kBK, tg::kBM, "A")) != TG_OK) return rc;
+  if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, tg::kBK, "B")) != TG_OK) return rc;
+  if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
+  l.M = static_cast<uint32_t>(M);
+  l.N = static_cast<uint32_t>(N);
+  l.K = static_cast<uint32_t>(K);
+  l.m_blocks = static_cast<uint32_t>((M + tg::kBM - 1) / tg::kBM);
+  l.n_blocks = static_cast<uint32_t>((N + tg::kBN - 1) / tg::kBN);
+  l.k_blocks = static_cast<uint32_t>((K + tg::kBK - 1) / tg::kBK);
+  l.group = tg::kGroup;
+  const uint64_t tiles = uint64_t(l.m_blocks) * l.n_blocks;
+  l.grid = static_cast<uint32_t>(tiles < uint64_t(sms) ? tiles : uint64_t(sms));
+  l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
+  l.trace = trace;
+  l.inject_skip_phase = inject;
+  cudaError_t e;
+  if (debug && (e = tg::clear_watchdog_status(s)) != cudaSuccess)
+    return fail_cuda("clearing the watchdog word", e);
+  if ((e = tg::launch_gemm(dtype, debug, l, s)) != cudaSuccess) return fail_cuda("GEMM launch", e);
+  if (debug) {
+    unsigned int st = 0;
+    if ((e = tg::read_and_clear_watchdog_status(&st, s)) != cudaSuccess)
+      return fail_cuda("GEMM execution", e);
+    if (st)
+      return fail(TG_ERR_TIMEOUT, "watchdog: a wait gave up (roles 0x%x: 1 producer, 2 MMA, "
+                  "4 epilogue, 8 shutdown)", st);
+  }
+  return TG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev, int64_t M, int64_t N,
+                       int64_t K, int dtype, void* stream) {
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, false, nullptr, 0, -1);
+}
+
+int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
+                             int64_t N, int64_t K, int dtype, void* stream, int32_t* trace_dev,
+                             uint64_t watchdog_ns, int64_t inject_skip_phase) {
+  if (trace_dev) {
+    int rc = check_device_ptr(trace_dev, "trace");
+    if (rc != TG_OK) return rc;
+  }
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, true, trace_dev, watchdog_ns,
+                   inject_skip_phase);
+}
+
+int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host) {
+  if (m_blocks < 1 || n_blocks < 1 || num_sms < 1 || group < 1)
+    return fail(TG_ERR_ARG, "m_blocks, n_blocks, num_sms and group must be >= 1");
+  if (int64_t(m_blocks) * n_blocks > kMaxDim) return fail(TG_ERR_ARG, "too many tiles");
+  if (!out_host) return fail(TG_ERR_ARG, "null output buffer");
+  const uint64_t rows = uint64_t(m_blocks) * n_blocks;
+  const size_t bytes = rows * 4 * sizeof(int32_t);
+  int32_t* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, bytes);
+  if (e != cudaSuccess) return fail_cuda("cudaMalloc", e);
+  e = tg::launch_tile_schedule(m_blocks, n_blocks, num_sms, group, d, nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(out_host, d, bytes, cudaMemcpyDeviceToHost);
+  cudaError_t e2 = cudaFree(d);
+  if (e != cudaSuccess) return fail_cuda("tile schedule", e);
+  if (e2 != cudaSuccess) return fail_cuda("cudaFree", e2);
+  return static_cast<int>(rows);
+}
+
+const char* tg_last_error(void) { return g_err; }
+
+int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* group) {
+  if (block_m) *block_m = tg::kBM;
+  if (block_n) *block_n = tg::kBN;
+  if (block_k) *block_k = tg::kBK;
+  if (stages) *stages = tg::kStages;
+  if (group) *group = tg::kGroup;
+  return TG_OK;
+}
+
+int tg_device_status(void* stream) {
+  unsigned int st = 0;
+  cudaError_t e = tg::read_and_clear_watchdog_status(&st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda("tg_device_status", e);
+  if (st) return fail(TG_ERR_TIMEOUT, "watchdog fired (roles 0x%x)", st);
+  return TG_OK;
+}
+
+int tg_gemm_persistent_host(const void* A_host, const void* B_host, void* C_host, void* A_dev,
+                            void* B_dev, void* C_dev, int64_t M, int64_t N, int64_t K, int dtype,
+                            void* stream) {
+  bool nothing = false;
+  int rc = validate(A_dev, B_dev, C_dev, M, N, K, dtype, &nothing);
+  if (rc != TG_OK || nothing) return rc;
+  if (!C_host || (K > 0 && (!A_host || !B_host))) return fail(TG_ERR_ARG, "null host pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (K > 0) {
+    if ((e = cudaMemcpyAsync(A_dev, A_host, uint64_t(M) * K * tg::kElemBytes,
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return fail_cuda("copy of A to the device", e);
+    if ((e = cudaMemcpyAsync(B_dev, B_host, uint64_t(K) * N * tg::kElemBytes,
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return fail_cuda("copy of B to the device", e);
+  }
+  if ((rc = tg_gemm_persistent(A_dev, B_dev, C_dev, M, N, K, dtype, stream)) != TG_OK) return rc;
+  if ((e = cudaMemcpyAsync(C_host, C_dev, uint64_t(M) * N * tg::kElemBytes,
+                           cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return fail_cuda("copy of C to the host", e);
+  return TG_OK;
+}
+
+}  // extern "C"

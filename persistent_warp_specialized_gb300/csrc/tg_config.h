@@ -1,0 +1,61 @@
+// tg_config.h -- compile-time tiling of the persistent warp-specialized GEMM.
+//
+// The pages leave block_M / block_N / block_K / num_stages / store_block_N open (they are
+// parameters of ``gemm_persistent`` in "[Feature] Introduce tile scheduler #2441",
+// gemm_tcgen5mma_ws_persistent.py, ``main``).  Values chosen for sm_103a:
+//   block_M = 128   the M of one cta_group::1 tcgen05.mma; TMEM lane i holds row i
+//   block_N = 256   the largest N of one tcgen05.mma; two fp32 accumulators of 256 columns
+//                   fill all 512 TMEM columns (the page's C_tmem_0 / C_tmem_1)
+//   block_K = 64    64 x 2 bytes = 128 bytes: exactly one row of the 128-byte swizzle atom
+//   num_stages = 4  4 x 48 KiB of operand ring; with 32 KiB of epilogue staging it fits in
+//                   the 227 KiB a CTA may use
+//   store_block_N = 64   the epilogue drains and stores 64 columns (128 bytes) at a time
+//   group = 8       the page's group_size of the grouped tile order
+// Warp roles (256 threads, as the page's ``threads=256``): warp 0 issues TMA loads, warp 1
+// issues tcgen05.mma, warp 2 owns the TMEM allocation, warps 4..7 are the epilogue (warp
+// 4 + q may only touch TMEM lanes 32q..32q+31).
+#pragma once
+
+#include <cstdint>
+
+namespace tg {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kEpiN = 64;
+constexpr int kGroup = 8;
+constexpr int kThreads = 256;
+constexpr int kUmmaK = 16;                 // K of one tcgen05.mma kind::f16
+constexpr int kEpiWarps = 4;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kFirstEpiWarp = 4;
+
+constexpr uint32_t kElemBytes = 2;
+constexpr uint32_t kABytes = kBM * kBK * kElemBytes;             // 16 KiB
+constexpr uint32_t kBBytes = kBK * kBN * kElemBytes;             // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;              // 48 KiB: expect_tx per stage
+constexpr uint32_t kBChunkCols = 64;                             // one 128-byte swizzle row of B
+constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * kElemBytes;  // 8 KiB
+constexpr uint32_t kEpiBufBytes = 32 * kEpiN * kElemBytes;       // 4 KiB: 32 rows x 128 bytes
+constexpr uint32_t kSmemAlignSlack = 1024;
+constexpr uint32_t kSmemBytes =
+    kSmemAlignSlack + kStages * kStageBytes + kEpiWarps * 2 * kEpiBufBytes;
+constexpr uint32_t kTmemCols = 512;
+
+static_assert(kBK * kElemBytes == 128, "block_K must span one 128-byte swizzle row");
+static_assert(kEpiN * kElemBytes == 128, "store_block_N must span one 128-byte swizzle row");
+static_assert(kBN % kBChunkCols == 0 && kBN % kEpiN == 0, "block_N tiling");
+static_assert(kBM == 128 && kBN % 16 == 0 && kBN <= 256, "tcgen05.mma cta_group::1 shape");
+static_assert(2 * kBN <= (int)kTmemCols, "two accumulators must fit in TMEM");
+static_assert(kSmemBytes + 256 <= 232448, "shared memory per CTA");
+
+// watchdog: bits of the per-device status word naming the role that gave up a wait
+constexpr uint32_t kRoleProducer = 1u;
+constexpr uint32_t kRoleMma = 2u;
+constexpr uint32_t kRoleEpilogue = 4u;
+constexpr uint32_t kRoleDrain = 8u;
+constexpr uint64_t kDefaultWatchdogNs = 1ull << 32;  // about 4.3 s
+
+}  // namespace tg

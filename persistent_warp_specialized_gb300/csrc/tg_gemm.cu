@@ -1,0 +1,115 @@
+// tg_gemm.cu -- instantiations and launchers of the sm_103a kernels behind the C ABI:
+// the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
+// tile-schedule inspection kernel, and the zero fill used when K == 0.
+#include "tg_gemm_kernel.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+
+namespace {
+
+// One thread per worker runs the scheduler the GEMM roles run and writes its rows
+// (worker, w, bx, by); rows are ordered by worker, then w.  Worker c owns
+// q + (c < r) tiles where total = q * P + r, so its first row is c * q + min(c, r).
+__global__ void tile_schedule_kernel(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
+                                     uint32_t group, int32_t* __restrict__ out) {
+  const uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= num_workers) return;
+  const uint32_t total = m_blocks * n_blocks;
+  const uint32_t q = total / num_workers;
+  const uint32_t r = total % num_workers;
+  uint64_t row = static_cast<uint64_t>(c) * q + (c < r ? c : r);
+  PersistentTileScheduler sched(m_blocks, n_blocks, group, num_workers);
+  sched.init(c);
+  while (sched.valid()) {
+    int32_t* o = out + 4 * row;
+    o[0] = static_cast<int32_t>(c);
+    o[1] = static_cast<int32_t>(sched.current_iter);
+    o[2] = static_cast<int32_t>(sched.m_idx);
+    o[3] = static_cast<int32_t>(sched.n_idx);
+    ++row;
+    sched.next_tile();
+  }
+}
+
+__global__ void zero_fill_kernel(uint4* __restrict__ dst, uint64_t n16) {
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += stride)
+    dst[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int DT, bool DEBUG>
+cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
+  GemmParams p;
+  p.M = l.M;
+  p.N = l.N;
+  p.K = l.K;
+  p.m_blocks = l.m_blocks;
+  p.n_blocks = l.n_blocks;
+  p.k_blocks = l.k_blocks;
+  p.group = l.group;
+  p.watchdog_ns = l.watchdog_ns;
+  p.trace = l.trace;
+  p.inject_skip_phase = l.inject_skip_phase;
+  gemm_persistent_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kSmemBytes, stream>>>(l.tmA, l.tmB,
+                                                                                 l.tmC, p);
+  return cudaGetLastError();
+}
+
+template <int DT, bool DEBUG>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_persistent_ws_kernel<DT, DEBUG>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+
+}  // namespace
+
+cudaError_t prepare_gemm_kernels() {
+  cudaError_t e;
+  if ((e = set_smem_attr<0, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<1, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<0, true>()) != cudaSuccess) return e;
+  return set_smem_attr<1, true>();
+}
+
+cudaError_t launch_gemm(int dtype, bool debug, const GemmLaunch& l, cudaStream_t stream) {
+  if (dtype == 0) return debug ? launch_one<0, true>(l, stream) : launch_one<0, false>(l, stream);
+  return debug ? launch_one<1, true>(l, stream) : launch_one<1, false>(l, stream);
+}
+
+cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {
+  const uint64_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  uint64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<uint4*>(C), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
+                                 uint32_t group, int32_t* out_dev, cudaStream_t stream) {
+  const uint32_t threads = 128;
+  const uint32_t blocks = (num_workers + threads - 1) / threads;
+  tile_schedule_kernel<<<blocks, threads, 0, stream>>>(m_blocks, n_blocks, num_workers, group,
+                                                       out_dev);
+  return cudaGetLastError();
+}
+
+cudaError_t clear_watchdog_status(cudaStream_t stream) {
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbolAsync(g_watchdog_status, &zero, sizeof(zero), 0,
+                                 cudaMemcpyHostToDevice, stream);
+}
+
+cudaError_t read_and_clear_watchdog_status(unsigned int* out, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_watchdog_status, sizeof(*out));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_watchdog_status, &zero, sizeof(zero));
+}
+
+}  // namespace tg

@@ -1,0 +1,336 @@
+// tg_gemm_kernel.cuh -- persistent, warp-specialized GEMM for sm_103a (tcgen05 + TMA).
+//
+// Structure ("[Feature] Introduce tile scheduler #2441", gemm_tcgen5mma_ws_persistent.py,
+// ``gemm_persistent``, and the sequence diagram of the PR conversation):
+//   * one CTA per SM (grid = min(#SMs, #tiles)) loops over output tiles of 128 x 256;
+//   * warp 0 (one lane): TMA producer.  For each tile and k-block, phase = w * k_blocks + k,
+//     slot s = phase % S: wait consumed[s] (parity ((phase / S) & 1) ^ 1), arm loaded[s]
+//     with the stage's byte count, load the A box (128 x 64) and four B boxes (64 x 64);
+//   * warp 1 (one lane): MMA issuer.  For tile w: wait tmem_empty[w & 1] (parity
+//     ((w / 2) & 1) ^ 1); for each k-block wait loaded[s] (parity (phase / S) & 1) and issue
+//     four tcgen05.mma 128 x 256 x 16 into accumulator w & 1, the first with accumulate off
+//     (clear_accum = k == 0); tcgen05.commit -> consumed[s] frees the slot when those MMAs
+//     are done.  After the k-loop, tcgen05.commit -> tmem_full[w & 1];
+//   * warps 4..7: epilogue.  Wait tmem_full[w & 1] (parity (w / 2) & 1), copy the 32 TMEM
+//     lanes of the warp to registers 64 columns at a time, release the accumulator
+//     (arrive tmem_empty[w & 1]) as soon as the last columns are in registers -- before
+//     the global stores, as on the page -- then convert to the output type, stage each
+//     32 x 64 chunk in shared memory (128-byte swizzle) and TMA-store it (store_block_N
+//     chunks through C_shared, the page's use_tma_store path).  The TMA store clips rows
+//     >= M and columns >= N, which is the boundary masking of partial edge tiles;
+//   * warp 2 allocates the 512 TMEM columns at start and frees them at exit.
+// Every role builds its own PersistentTileScheduler and follows ``while valid(): ...
+// next_tile()``; the scheduler's ``current_iter`` is the single clock w.
+//
+// Every wait is bounded (watchdog): a wait that has not completed after ``watchdog_ns``
+// sets the per-device status word and a CTA-wide abort flag, every role then leaves its
+// loop at its next wait, the producer waits (bounded) for the loads it still has in
+// flight, the MMA thread waits (bounded) for its MMAs, the epilogue waits for its stores,
+// and the CTA frees TMEM and exits.  The host reads the status word (tg_device_status).
+//
+// Shared memory layout (dynamic, 1024-byte aligned): stage s at s * 48 KiB holds A
+// (128 rows x 128 bytes, K-major, 128-byte swizzle: row r's 16-byte chunk c sits at chunk
+// c ^ (r % 8)) followed by B as four 8 KiB column chunks (64 K-rows x 64 N-columns each,
+// N-major, same swizzle); then 8 epilogue staging buffers (2 per epilogue warp) of
+// 32 rows x 128 bytes.  This header is included by exactly one translation unit.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "tg_config.h"
+#include "tg_ptx.cuh"
+#include "tg_tile_scheduler.cuh"
+
+namespace tg {
+
+struct GemmParams {
+  uint32_t M, N, K;
+  uint32_t m_blocks, n_blocks, k_blocks, group;
+  uint64_t watchdog_ns;
+  int32_t* trace;              // debug instantiation only; may be null
+  int64_t inject_skip_phase;   // debug instantiation only; -1 = none
+};
+
+// Per-device status word of the watchdog (bits: kRole*).  Read and cleared by the host.
+__device__ unsigned int g_watchdog_status = 0;
+
+struct __align__(8) GemmCtl {
+  uint64_t loaded[kStages];
+  uint64_t consumed[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Wait for the phase of parity ``parity`` of ``bar``; false if the CTA is aborting or the
+// wait ran past ``limit_ns`` (then this thread raises the abort and records ``role``).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, uint64_t limit_ns,
+                                              uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(&g_watchdog_status, role);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while shutting down (ignores the abort flag).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(&g_watchdog_status, role);
+      return false;
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack_out(uint32_t lo_bits, uint32_t hi_bits) {
+  const float lo = __uint_as_float(lo_bits);
+  const float hi = __uint_as_float(hi_bits);
+  if constexpr (DT == 1) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+// DT: 0 = fp16, 1 = bf16 (input and output).  DEBUG adds the tile trace and fault injection.
+template <int DT, bool DEBUG>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_persistent_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB,
+                              const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ GemmCtl ctl;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA0 = sbase;                     // A of stage s: sA0 + s * kStageBytes
+  const uint32_t sB0 = sbase + kABytes;           // B of stage s: sB0 + s * kStageBytes
+  const uint32_t sEpi = sbase + kStages * kStageBytes;
+
+  const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
+  const uint32_t bar_consumed = smem_u32(&ctl.consumed[0]);
+  const uint32_t bar_tmem_full = smem_u32(&ctl.tmem_full[0]);
+  const uint32_t bar_tmem_empty = smem_u32(&ctl.tmem_empty[0]);
+  const uint32_t bar_drain = smem_u32(&ctl.drain);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_loaded + 8u * s, 1);
+      mbar_init(bar_consumed + 8u * s, 1);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tmem_full + 8u * b, 1);
+      mbar_init(bar_tmem_empty + 8u * b, kEpiThreads);
+    }
+    mbar_init(bar_drain, 1);
+    ctl.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  __syncwarp();
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tcgen05_fence_before_sync();
+  __syncthreads();
+  tcgen05_fence_after_sync();
+
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+  const uint64_t limit = p.watchdog_ns;
+  const uint64_t k_blocks = p.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+      sched.init(blockIdx.x);
+      uint32_t pending = 0;       // stages whose latest fill may still be in flight
+      uint32_t pending_par = 0;   // parity of that fill, one bit per stage
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint64_t w = sched.current_iter;
+        const int32_t m0 = static_cast<int32_t>(sched.m_idx) * kBM;
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx) * kBN;
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = w * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kStages) & 1u);
+          if (!wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, limit, kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          pending &= ~(1u << s);
+          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+            continue;  // injected fault: this phase is never filled
+          const uint32_t full = bar_loaded + 8u * s;
+          mbar_arrive_expect_tx(full, kStageBytes);
+          const int32_t kx = static_cast<int32_t>(k) * kBK;
+          tma_load_2d(sA0 + s * kStageBytes, &tmA, full, kx, m0);
+#pragma unroll
+          for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
+            tma_load_2d(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
+                        n0 + static_cast<int32_t>(c * kBChunkCols), kx);
+          pending |= 1u << s;
+          pending_par = (pending_par & ~(1u << s)) | (par << s);
+        }
+        sched.next_tile();
+      }
+      if (!ok) {
+        for (uint32_t s = 0; s < kStages; ++s)
+          if ((pending >> s) & 1u)
+            wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+      }
+    }
+    __syncwarp();   // reconverge before the CTA-wide barrier below
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(DT, kBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+      sched.init(blockIdx.x);
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint32_t w = sched.current_iter;
+        const uint32_t buf = w & 1u;
+        if (!wait_or_abort(bar_tmem_empty + 8u * buf, ((w >> 1) & 1u) ^ 1u, abort_flag, limit,
+                           kRoleMma)) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * kBN;
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kStages) & 1u);
+          if (!wait_or_abort(bar_loaded + 8u * s, par, abort_flag, limit, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after_sync();
+          const uint32_t a_addr = sA0 + s * kStageBytes;
+          const uint32_t b_addr = sB0 + s * kStageBytes;
+#pragma unroll
+          for (uint32_t kk = 0; kk < kBK / kUmmaK; ++kk) {
+            // A: K-major, advance 16 elements = 32 bytes inside the swizzle row;
+            //    SBO = 1024 bytes between 8-row groups.
+            // B: N-major, advance 16 K-rows = 2048 bytes; LBO = 8 KiB between 64-column
+            //    chunks, SBO = 1024 bytes between 8-row groups.
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kBChunkBytes, 1024);
+            umma_f16(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+          }
+          umma_commit(bar_consumed + 8u * s);
+        }
+        if (!ok) break;
+        umma_commit(bar_tmem_full + 8u * buf);
+        sched.next_tile();
+      }
+      // every MMA this thread issued has finished before TMEM can be released
+      umma_commit(bar_drain);
+      wait_bounded(bar_drain, 0, limit, kRoleDrain);
+    }
+    __syncwarp();
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp - kFirstEpiWarp;       // TMEM lanes 32q .. 32q + 31
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+    sched.init(blockIdx.x);
+    uint32_t chunk = 0;
+    while (sched.valid()) {
+      const uint32_t w = sched.current_iter;
+      const uint32_t buf = w & 1u;
+      const bool got = wait_or_abort(bar_tmem_full + 8u * buf, (w >> 1) & 1u, abort_flag, limit,
+                                     kRoleEpilogue);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tcgen05_fence_after_sync();
+      const int32_t row0 = static_cast<int32_t>(sched.m_idx) * kBM + static_cast<int32_t>(q) * 32;
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN;
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kBN;
+#pragma unroll 1
+      for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+        uint32_t v[64];
+        tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
+        if (j == kBN / kEpiN - 1) {
+          // accumulator fully in registers: hand it back to the MMA warp before storing
+          tcgen05_fence_before_sync();
+          mbar_arrive(bar_tmem_empty + 8u * buf);
+        }
+        const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
+        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read sbuf is done
+        __syncwarp();
+        const uint32_t row_addr = sbuf + lane * 128u;
+#pragma unroll
+        for (uint32_t c = 0; c < 8; ++c) {
+          st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4),
+                       pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
+                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
+                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
+                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t x = col0 + static_cast<int32_t>(j * kEpiN);
+          if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
+            tma_store_2d(&tmC, sbuf, x, row0);
+          bulk_commit_group();   // one group per chunk, empty when the chunk is outside C
+        }
+        __syncwarp();   // converged for the next warp-collective tcgen05.ld
+      }
+      if (DEBUG && p.trace != nullptr && q == 0 && lane == 0) {
+        int32_t* tr = p.trace + 4ull * sched.linear_idx;
+        tr[0] = static_cast<int32_t>(blockIdx.x);
+        tr[1] = static_cast<int32_t>(w);
+        tr[2] = static_cast<int32_t>(sched.m_idx);
+        tr[3] = static_cast<int32_t>(sched.n_idx);
+      }
+      sched.next_tile();
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tcgen05_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tcgen05_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tg

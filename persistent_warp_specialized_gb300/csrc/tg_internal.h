@@ -1,0 +1,34 @@
+// tg_internal.h -- interface between the C-ABI translation unit (tg_api.cu) and the
+// translation unit that holds the kernels (tg_gemm.cu).  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace tg {
+
+struct GemmLaunch {
+  CUtensorMap tmA, tmB, tmC;
+  uint32_t M, N, K;
+  uint32_t m_blocks, n_blocks, k_blocks, group;
+  uint32_t grid;
+  uint64_t watchdog_ns;
+  int32_t* trace;
+  int64_t inject_skip_phase;
+};
+
+// Sets the dynamic shared-memory limit of every GEMM instantiation on the current device.
+cudaError_t prepare_gemm_kernels();
+// dtype 0 = fp16, 1 = bf16
+cudaError_t launch_gemm(int dtype, bool debug, const GemmLaunch& l, cudaStream_t stream);
+// C[0 .. bytes) = 0 (bytes a multiple of 16, C 16-byte aligned)
+cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream);
+cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
+                                 uint32_t group, int32_t* out_dev, cudaStream_t stream);
+cudaError_t clear_watchdog_status(cudaStream_t stream);
+// synchronises ``stream``, returns the status word in *out and clears it
+cudaError_t read_and_clear_watchdog_status(unsigned int* out, cudaStream_t stream);
+
+}  // namespace tg

@@ -1,0 +1,68 @@
+// tg_tile_scheduler.cuh -- the persistent tile scheduler, one instance per warp role.
+//
+// "[Feature] Introduce tile scheduler #2441" replaces the hand-written
+// ``for w in T.unroll(waves): tile_id = sm_num * w + block_id`` loop of
+// gemm_tcgen5mma_ws_persistent.py with ``sched = T.PersistentTileScheduler(prefix, m_blocks,
+// n_blocks, swizzle_size=group_size)``, ``sched.init(block_id)``, ``while sched.valid():``
+// ... ``sched.next_tile()``.  Each role (TMA producer, MMA issuer, epilogue) owns one
+// instance; the scheduler holds the only iteration clock: ``current_iter`` is the wave index
+// w that drives the pipeline phase and the w & 1 accumulator choice, and ``m_idx``/``n_idx``
+// are the tile coordinates.  Because every role's instance is built from the same
+// arguments and advanced once per tile, all roles see the same (w, bx, by) sequence.
+//
+// Linear ids are grid-strided (worker c takes c, c + P, c + 2P, ...) and decoded in the
+// grouped order of the page, bx = (t / g) % m_blocks, by = t % g + (t / g) / m_blocks * g,
+// which walks panels of g N-tiles top to bottom for L2 reuse.  The page only meets full
+// panels (it asserts n_blocks % (2 * group_size) == 0); here the last panel, when
+// n_blocks % g != 0, is narrowed to its real width so the decode stays a bijection on
+// [0, m_blocks * n_blocks).  With p = t / (m_blocks * g), width = min(g, n_blocks - p * g)
+// and u = t - p * m_blocks * g, a tile is (u / width, p * g + u % width); on full panels
+// this equals the page's formula term for term.
+#pragma once
+
+#include <cstdint>
+
+namespace tg {
+
+struct PersistentTileScheduler {
+  uint32_t m_blocks, n_blocks, group, num_workers, total;
+  uint32_t current_iter;  // w: tiles this worker has already taken
+  uint32_t linear_idx;    // worker + w * num_workers
+  uint32_t m_idx, n_idx;  // decoded tile (valid only while valid())
+
+  __host__ __device__ PersistentTileScheduler(uint32_t m, uint32_t n, uint32_t g, uint32_t p)
+      : m_blocks(m), n_blocks(n), group(g), num_workers(p), total(m * n),
+        current_iter(0), linear_idx(0), m_idx(0), n_idx(0) {}
+
+  __host__ __device__ static void coord(uint32_t t, uint32_t m_blocks, uint32_t n_blocks,
+                                        uint32_t group, uint32_t& bx, uint32_t& by) {
+    const uint32_t panel_tiles = m_blocks * group;
+    const uint32_t p = t / panel_tiles;
+    const uint32_t first_col = p * group;
+    const uint32_t left = n_blocks - first_col;
+    const uint32_t width = left < group ? left : group;
+    const uint32_t u = t - p * panel_tiles;
+    bx = u / width;
+    by = first_col + u % width;
+  }
+
+  __host__ __device__ void decode() {
+    if (linear_idx < total) coord(linear_idx, m_blocks, n_blocks, group, m_idx, n_idx);
+  }
+
+  __host__ __device__ void init(uint32_t worker) {
+    current_iter = 0;
+    linear_idx = worker;
+    decode();
+  }
+
+  __host__ __device__ bool valid() const { return linear_idx < total; }
+
+  __host__ __device__ void next_tile() {
+    ++current_iter;
+    linear_idx += num_workers;
+    decode();
+  }
+};
+
+}  // namespace tg

@@ -1,0 +1,90 @@
+"""The C-ABI library builds, loads and exports every entry point include/tg.h declares.
+
+No GPU is needed: only argument checks that return before any CUDA call are exercised.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tg_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from persistent_warp_specialized_gb300 import _build
+
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("tg_gemm_persistent", "tg_tile_schedule", "tg_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+
+
+def test_binding_covers_every_declared_symbol():
+    import persistent_warp_specialized_gb300 as tg
+
+    assert sorted(tg.EXPORTED) == declared_functions()
+
+
+def test_config_query(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    cfg = tg.tg_gemm_config()
+    assert cfg == {"block_m": 128, "block_n": 256, "block_k": 64, "stages": 4, "group": 8}
+
+
+def test_host_side_rejections_need_no_gpu(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent(16, 16, 16, 8, 8, 8, 7, stream=0)      # unknown dtype
+    assert e.value.code == tg.TG_ERR_ARG
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent(16, 16, 16, -1, 8, 8, "bf16", stream=0)  # negative size
+    assert e.value.code == tg.TG_ERR_ARG
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent(16, 16, 16, 8, 12, 8, "bf16", stream=0)  # N % 8 != 0
+    assert e.value.code == tg.TG_ERR_ALIGN
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent(16, 24, 8, 8, 8, 8, "f16", stream=0)     # C not 16-byte aligned
+    assert e.value.code == tg.TG_ERR_ALIGN
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent(None, 16, 16, 8, 8, 8, "f16", stream=0)  # null A
+    assert e.value.code == tg.TG_ERR_ARG
+    # empty problems are a successful no-op
+    assert tg.tg_gemm_persistent(None, None, None, 0, 8, 8, "f16", stream=0) == 0
+    assert tg.tg_gemm_persistent(None, None, None, 8, 0, 8, "f16", stream=0) == 0
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_tile_schedule(0, 3, 148, 8)
+    assert e.value.code == tg.TG_ERR_ARG
+    assert "must be" in tg.tg_last_error()
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "persistent_warp_specialized_gb300")
+    pat = re.compile(r"^\s*(from\s+oracle\b|import\s+oracle\b)|oracle/", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not pat.search(text), f

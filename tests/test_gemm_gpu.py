@@ -1,0 +1,142 @@
+"""GPU parity: tg_gemm_persistent against the CPU oracle, element by element.
+
+Small shapes span several tiles and ragged tails in M, N and K (the kernel tiles
+128 x 256 x 64), integer-valued inputs must be bit-exact (every fp32 partial sum is an
+exact integer, so any accumulation order gives the same bits: a wrong slot, phase or
+accumulator shows up as a wrong value), and the degenerate cases have closed forms.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import persistent_warp_specialized_gb300 as tg
+from persistent_warp_specialized_gb300 import workloads as wl
+from oracle import formats
+
+from gpu_helpers import assert_within_tolerance, ensure_library, oracle_bits, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+SHAPES = [
+    (128, 256, 64),     # exactly one tile, one k-block
+    (1, 8, 8),          # smallest legal problem
+    (300, 520, 200),    # 3 x 3 tiles, ragged M, N and K
+    (129, 264, 72),     # one row / one 8-column strip past a tile, K tail of 8
+    (257, 776, 136),
+    (640, 1024, 320),   # 5 x 4 tiles, full
+    (1000, 8, 16),      # a single column strip
+    (8, 4000, 1032),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_small_shapes_match_oracle(shape, dtype):
+    M, N, K = shape
+    a, b = wl.make_inputs(M, N, K, dtype, "uniform", seed=M + N + K)
+    assert_within_tolerance(run_gpu(a, b, dtype), oracle_bits(a, b, dtype), dtype, str(shape))
+
+
+@pytest.mark.parametrize("dtype,K", [("f16", 512), ("bf16", 64), ("f16", 200), ("bf16", 40)])
+def test_integer_inputs_are_bit_exact(dtype, K):
+    # entries in [-2, 2]: |C| <= 4K, exact in the output type (f16: 2048, bf16: 256)
+    M, N = 300, 776
+    a, b = wl.small_int_inputs(M, N, K, dtype, seed=K)
+    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_many_tiles_per_cta_with_short_k(dtype):
+    # 32 x 16 = 512 tiles (> 3 per SM); k_blocks = 3 is not a multiple of the 4 stages, the
+    # case where indexing the consumer's slot by k instead of the phase goes wrong
+    M, N, K = 4096, 4096, 192
+    a, b = wl.small_int_inputs(M, N, K, dtype, lo=-1, hi=1, seed=9)
+    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_k_shorter_than_one_block_many_tiles(dtype):
+    M, N, K = 2048, 2048, 8          # k_blocks = 1: every phase is a new tile
+    a, b = wl.small_int_inputs(M, N, K, dtype, seed=4)
+    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_identity_reproduces_operand(dtype):
+    n = 384
+    eye = torch.eye(n, dtype=wl.TORCH_DTYPES[dtype])
+    x, _ = wl.make_inputs(n, 8, 520, dtype, "uniform", seed=2)      # [384, 520]
+    assert np.array_equal(run_gpu(eye, x, dtype), wl.bits(x))        # I . X = X
+    y, _ = wl.make_inputs(300, 8, n, dtype, "uniform", seed=3)       # [300, 384]
+    assert np.array_equal(run_gpu(y, eye, dtype), wl.bits(y))        # Y . I = Y
+
+
+@pytest.mark.parametrize("dtype,K", [("f16", 2048), ("bf16", 8192)])
+def test_all_ones_give_k(dtype, K):
+    M, N = 256, 512
+    t = wl.TORCH_DTYPES[dtype]
+    c = run_gpu(torch.ones((M, K), dtype=t), torch.ones((K, N), dtype=t), dtype)
+    assert np.array_equal(formats.decode(c, dtype), np.full((M, N), float(K)))
+
+
+def test_k_zero_gives_zeros():
+    c = torch.full((64, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    tg.tg_gemm_persistent(a, b, c, 64, 64, 0, "bf16")
+    torch.cuda.synchronize()
+    assert bool((c == 0).all())
+
+
+def test_runs_on_a_side_stream():
+    M, N, K = 500, 600, 264
+    a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=21)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = run_gpu(a, b, "bf16", stream=s)
+    assert_within_tolerance(got, oracle_bits(a, b, "bf16"), "bf16", "side stream")
+
+
+def test_repeated_calls_are_deterministic():
+    M, N, K = 1024, 1024, 1024
+    a, b = wl.make_inputs(M, N, K, "bf16", "normal", seed=5)
+    first = run_gpu(a, b, "bf16")
+    for _ in range(3):
+        assert np.array_equal(run_gpu(a, b, "bf16"), first)
+
+
+def test_host_entry_point_round_trip():
+    M, N, K = 700, 1032, 520
+    a, b = wl.make_inputs(M, N, K, "f16", "uniform", seed=17)
+    a_h, b_h = a.pin_memory(), b.pin_memory()
+    c_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    a_d = torch.empty_like(a_h, device="cuda")
+    b_d = torch.empty_like(b_h, device="cuda")
+    c_d = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    tg.tg_gemm_persistent_host(a_h, b_h, c_h, a_d, b_d, c_d, M, N, K, "f16")
+    torch.cuda.synchronize()
+    assert_within_tolerance(wl.bits(c_h), oracle_bits(a, b, "f16"), "f16", "host entry")
+
+
+def test_rejections_with_a_gpu():
+    a = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    host = torch.zeros((64, 64), dtype=torch.bfloat16)
+    with pytest.raises(tg.TgError) as e:                  # host memory where device is required
+        tg.tg_gemm_persistent(host, b, a, 64, 64, 64, "bf16")
+    assert e.value.code == tg.TG_ERR_ARG
+    with pytest.raises(tg.TgError) as e:                  # C aliases A
+        tg.tg_gemm_persistent(a, b, a, 64, 64, 64, "bf16")
+    assert e.value.code == tg.TG_ERR_ARG
+    big = torch.zeros(64 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tg.TgError) as e:                  # misaligned by 2 bytes
+        tg.tg_gemm_persistent(big.data_ptr() + 2, b, a, 64, 64, 64, "bf16")
+    assert e.value.code == tg.TG_ERR_ALIGN
+    torch.cuda.synchronize()

@@ -1,0 +1,95 @@
+"""GPU: the device tile scheduler against the oracle's brute-force enumeration (bit-exact),
+the GEMM kernel's own trace against the same enumeration, and the watchdog.
+"""
+
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import persistent_warp_specialized_gb300 as tg
+from persistent_warp_specialized_gb300 import workloads as wl
+from oracle import schedule
+
+from gpu_helpers import assert_within_tolerance, ensure_library, oracle_bits
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def test_schedule_brute_force_grids():
+    for m, n, g, p in itertools.product([1, 2, 5, 8, 13, 32], [1, 3, 4, 9, 16, 28],
+                                        [1, 3, 8], [1, 7, 148, 160]):
+        assert tg.tg_tile_schedule(m, n, p, g) == schedule.enumerate_schedule(m, n, p, g), (m, n, g, p)
+
+
+@pytest.mark.parametrize("name", sorted(f for f in os.listdir(GOLDEN) if f.startswith("schedule_")))
+def test_schedule_matches_stored_fixture(name):
+    meta = {}
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        if line.startswith("#"):
+            meta.update(dict(t.split("=") for t in line[1:].split() if "=" in t))
+            continue
+        rows.append(tuple(int(x) for x in line.split()))
+    got = tg.tg_tile_schedule(int(meta["m_blocks"]), int(meta["n_blocks"]), int(meta["workers"]),
+                              int(meta["group"]))
+    assert got == rows
+
+
+def test_config1_schedule_148_workers():
+    # the 256^3 workload: 2 x 1 tiles over 148 workers, group 8
+    assert tg.tg_tile_schedule(2, 1, wl.SCHEDULE_CHECK_WORKERS, wl.SCHEDULE_CHECK_GROUP) == [
+        (0, 0, 0, 0), (1, 0, 1, 0)]
+
+
+@pytest.mark.parametrize("M,N,K", [(4000, 7000, 256), (8192, 8192, 64), (1024, 1024, 1024), (256, 256, 256)])
+def test_kernel_followed_the_schedule(M, N, K):
+    # the epilogue of the real GEMM records (cta, w, bx, by) for every tile it stored
+    cfg = tg.tg_gemm_config()
+    m_blocks = -(-M // cfg["block_m"])
+    n_blocks = -(-N // cfg["block_n"])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    workers = min(sms, m_blocks * n_blocks)
+    a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=M)
+    a_d, b_d = a.cuda(), b.cuda()
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    trace = torch.full((m_blocks * n_blocks, 4), -1, dtype=torch.int32, device="cuda")
+    assert tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", trace=trace) == 0
+    want = schedule.enumerate_schedule(m_blocks, n_blocks, workers, cfg["group"])
+    by_tile = {}
+    for (cta, w, bx, by) in want:
+        by_tile[cta + w * workers] = (cta, w, bx, by)
+    got = trace.cpu().numpy()
+    for t in range(m_blocks * n_blocks):
+        assert tuple(int(v) for v in got[t]) == by_tile[t], t
+    # the debug build computes the same product
+    assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "debug build")
+
+
+def test_watchdog_fires_and_context_survives():
+    # CTA 0's producer never fills pipeline phase 5: the MMA role's wait on it cannot
+    # complete, the 20 ms watchdog must end every role and report TG_ERR_TIMEOUT
+    M, N, K = 512, 512, 1024
+    a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=1)
+    a_d, b_d = a.cuda(), b.cuda()
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", watchdog_ns=20_000_000,
+                                    inject_skip_phase=5)
+    assert e.value.code == tg.TG_ERR_TIMEOUT
+    assert "watchdog" in str(e.value)
+    # the context is intact: the status word was cleared and the next GEMM is correct
+    assert tg.tg_device_status() == 0
+    tg.tg_gemm_persistent(a_d, b_d, c, M, N, K, "bf16")
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "after watchdog")
