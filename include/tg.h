@@ -38,6 +38,14 @@ extern "C" {
 /* element types: input, output and (internally) fp32 accumulation */
 enum { TG_F16 = 0, TG_BF16 = 1 };
 
+/* kernel variants (tg_gemm_persistent_ex, tg_gemm_persistent_debug) */
+enum {
+  TG_VARIANT_AUTO = 0,    /* the library's choice for the problem (what tg_gemm_persistent runs) */
+  TG_VARIANT_SINGLE = 1,  /* one CTA per 128 x 256 output tile, tcgen05 cta_group::1 */
+  TG_VARIANT_PAIR = 2     /* a CTA pair per 256 x 256 output tile, tcgen05 cta_group::2
+                             ("[Feature] Introduce tile scheduler #2441", gemm_persistent_2cta) */
+};
+
 /* status codes */
 enum {
   TG_OK = 0,
@@ -59,6 +67,14 @@ enum {
  */
 int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
                        int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
+/*
+ * tg_gemm_persistent_ex -- tg_gemm_persistent with an explicit kernel variant (TG_VARIANT_*).
+ * Same arguments, rules and results; TG_ERR_ARG for an unknown variant.  The pair variant
+ * walks ceil(M/256) x ceil(N/256) tiles with one scheduler worker per CTA pair.
+ */
+int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
+                          int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant);
 
 /*
  * tg_tile_schedule -- the tile order the GEMM kernel follows, for inspection.
@@ -86,17 +102,19 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
 
 /*
  * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
- *   trace_dev: NULL or a device buffer of 4 * m_blocks * n_blocks int32; row t (t = the
- *     linear tile id) receives (cta, w, bx, by) as the epilogue of the CTA that stored tile t
- *     saw them -- evidence that the kernel followed the schedule of tg_tile_schedule.
+ *   variant: TG_VARIANT_* as in tg_gemm_persistent_ex.
+ *   trace_dev: NULL or a device buffer of 4 int32 per output tile of the variant (128 x 256
+ *     tiles for SINGLE, 256 x 256 for PAIR); row t (t = the linear tile id) receives
+ *     (worker, w, bx, by) as the epilogue that stored tile t saw them (worker = CTA, or CTA
+ *     pair) -- evidence that the kernel followed the schedule of tg_tile_schedule.
  *   watchdog_ns: limit for every wait inside the kernel (0 = the default of about 4 s).
- *   inject_skip_phase: -1 for none; otherwise CTA 0's producer never fills that pipeline
- *     phase, so the MMA role's wait on it cannot complete: the watchdog must fire, every
+ *   inject_skip_phase: -1 for none; otherwise CTA 0's producer never arms or fills that
+ *     pipeline phase, so the MMA role's wait on it cannot complete: the watchdog must fire, every
  *     role must stop, and the call must return TG_ERR_TIMEOUT with the context intact.
  * Synchronises ``stream``.  Returns TG_OK, TG_ERR_TIMEOUT or another error.
  */
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev,
-                             int64_t M, int64_t N, int64_t K, int dtype, void* stream,
+                             int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant,
                              int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase);
 
 /*

@@ -22,11 +22,16 @@ TG_ERR_ARG = -1
 TG_ERR_ALIGN = -2
 TG_ERR_CUDA = -3
 TG_ERR_TIMEOUT = -4
+TG_VARIANT_AUTO = 0
+TG_VARIANT_SINGLE = 1
+TG_VARIANT_PAIR = 2
+VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
 
 EXPORTED = (
     "tg_gemm_persistent",
+    "tg_gemm_persistent_ex",
     "tg_tile_schedule",
     "tg_last_error",
     "tg_gemm_config",
@@ -57,6 +62,8 @@ def load_library(path=LIB_PATH):
     vp, i64, i32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
     lib.tg_gemm_persistent.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.tg_gemm_persistent.restype = i32
+    lib.tg_gemm_persistent_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32]
+    lib.tg_gemm_persistent_ex.restype = i32
     lib.tg_tile_schedule.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.tg_tile_schedule.restype = i32
     lib.tg_last_error.argtypes = []
@@ -64,7 +71,8 @@ def load_library(path=LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
     lib.tg_gemm_config.restype = i32
-    lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, u64, i64]
+    lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
+                                             i64]
     lib.tg_gemm_persistent_debug.restype = i32
     lib.tg_device_status.argtypes = [vp]
     lib.tg_device_status.restype = i32
@@ -116,11 +124,21 @@ def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
 
 
-def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, trace=None, watchdog_ns=0,
-                             inject_skip_phase=-1):
+def _variant(v):
+    return VARIANTS[v] if isinstance(v, str) else int(v)
+
+
+def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto"):
+    """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair")."""
+    return _check(load_library().tg_gemm_persistent_ex(
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _variant(variant)))
+
+
+def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
+                             watchdog_ns=0, inject_skip_phase=-1):
     return _check(load_library().tg_gemm_persistent_debug(
-        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _ptr(trace),
-        watchdog_ns, inject_skip_phase))
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _variant(variant),
+        _ptr(trace), watchdog_ns, inject_skip_phase))
 
 
 def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,

@@ -57,13 +57,14 @@ EncodeTiledFn encode_fn() {
 struct DeviceInfo {
   int state = 0;  // 0 unknown, 1 ready, -1 unsupported
   int sms = 0;
+  int max_pairs = 0;  // CTA pairs of the pair kernel resident at once
   char why[256] = "";
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int device_ready(int* sms_out) {
+int device_ready(int* sms_out, int* max_pairs_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
@@ -80,8 +81,8 @@ int device_ready(int* sms_out) {
       d.state = -1;
       snprintf(d.why, sizeof(d.why), "device %d is sm_%d%d; this library is built for sm_103a",
                dev, major, minor);
-    } else if ((e = tg::prepare_gemm_kernels()) != cudaSuccess) {
-      return fail_cuda("cudaFuncSetAttribute(MaxDynamicSharedMemorySize)", e);
+    } else if ((e = tg::prepare_gemm_kernels(&d.max_pairs)) != cudaSuccess) {
+      return fail_cuda("preparing the GEMM kernels (shared memory limit, cluster occupancy)", e);
     } else {
       d.state = 1;
       d.sms = sms;
@@ -89,6 +90,7 @@ int device_ready(int* sms_out) {
   }
   if (d.state < 0) return fail(TG_ERR_CUDA, "%s", d.why);
   if (sms_out) *sms_out = d.sms;
+  if (max_pairs_out) *max_pairs_out = d.max_pairs;
   return TG_OK;
 }
 
@@ -167,13 +169,25 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
   return TG_OK;
 }
 
+// The variant TG_VARIANT_AUTO resolves to.
+int auto_variant(int64_t /*M*/, int64_t /*N*/, int64_t /*K*/, int max_pairs) {
+  (void)max_pairs;
+  return TG_VARIANT_SINGLE;
+}
+
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
-              void* stream, bool debug, int32_t* trace, uint64_t watchdog_ns, int64_t inject) {
+              void* stream, int variant, bool debug, int32_t* trace, uint64_t watchdog_ns,
+              int64_t inject) {
+  if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
+    return fail(TG_ERR_ARG, "unknown variant %d", variant);
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
   if (rc != TG_OK || nothing) return rc;
-  int sms = 0;
-  if ((rc = device_ready(&sms)) != TG_OK) return rc;
+  int sms = 0, max_pairs = 0;
+  if ((rc = device_ready(&sms, &max_pairs)) != TG_OK) return rc;
+  if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
+  if (variant == TG_VARIANT_PAIR && max_pairs < 1)
+    return fail(TG_ERR_CUDA, "no CTA pair of the pair kernel fits on this device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) {
     cudaError_t e = tg::launch_zero_fill(C, uint64_t(M) * N * tg::kElemBytes, s);
@@ -186,19 +200,26 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
-  l.m_blocks = static_cast<uint32_t>((M + tg::kBM - 1) / tg::kBM);
+  const int64_t tile_m = variant == TG_VARIANT_PAIR ? tg::kPairBM : tg::kBM;
+  l.m_blocks = static_cast<uint32_t>((M + tile_m - 1) / tile_m);
   l.n_blocks = static_cast<uint32_t>((N + tg::kBN - 1) / tg::kBN);
   l.k_blocks = static_cast<uint32_t>((K + tg::kBK - 1) / tg::kBK);
   l.group = tg::kGroup;
   const uint64_t tiles = uint64_t(l.m_blocks) * l.n_blocks;
-  l.grid = static_cast<uint32_t>(tiles < uint64_t(sms) ? tiles : uint64_t(sms));
+  if (variant == TG_VARIANT_PAIR) {
+    const uint64_t pairs = tiles < uint64_t(max_pairs) ? tiles : uint64_t(max_pairs);
+    l.grid = static_cast<uint32_t>(2 * pairs);
+  } else {
+    l.grid = static_cast<uint32_t>(tiles < uint64_t(sms) ? tiles : uint64_t(sms));
+  }
   l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
   l.trace = trace;
   l.inject_skip_phase = inject;
   cudaError_t e;
   if (debug && (e = tg::clear_watchdog_status(s)) != cudaSuccess)
     return fail_cuda("clearing the watchdog word", e);
-  if ((e = tg::launch_gemm(dtype, debug, l, s)) != cudaSuccess) return fail_cuda("GEMM launch", e);
+  if ((e = tg::launch_gemm(dtype, debug, variant, l, s)) != cudaSuccess)
+    return fail_cuda("GEMM launch", e);
   if (debug) {
     unsigned int st = 0;
     if ((e = tg::read_and_clear_watchdog_status(&st, s)) != cudaSuccess)
@@ -216,18 +237,24 @@ extern "C" {
 
 int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev, int64_t M, int64_t N,
                        int64_t K, int dtype, void* stream) {
-  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, false, nullptr, 0, -1);
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, TG_VARIANT_AUTO, false, nullptr,
+                   0, -1);
+}
+
+int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
+                          int64_t N, int64_t K, int dtype, void* stream, int variant) {
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, false, nullptr, 0, -1);
 }
 
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
-                             int64_t N, int64_t K, int dtype, void* stream, int32_t* trace_dev,
-                             uint64_t watchdog_ns, int64_t inject_skip_phase) {
+                             int64_t N, int64_t K, int dtype, void* stream, int variant,
+                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase) {
   if (trace_dev) {
     int rc = check_device_ptr(trace_dev, "trace");
     if (rc != TG_OK) return rc;
   }
-  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, true, trace_dev, watchdog_ns,
-                   inject_skip_phase);
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, true, trace_dev,
+                   watchdog_ns, inject_skip_phase);
 }
 
 int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host) {

@@ -51,6 +51,22 @@ static_assert(kBM == 128 && kBN % 16 == 0 && kBN <= 256, "tcgen05.mma cta_group:
 static_assert(2 * kBN <= (int)kTmemCols, "two accumulators must fit in TMEM");
 static_assert(kSmemBytes + 256 <= 232448, "shared memory per CTA");
 
+// CTA-pair variant (tcgen05 cta_group::2, the page's gemm_persistent_2cta): a cluster of two
+// CTAs computes a 256 x 256 output tile.  CTA r of the pair loads A rows [128r, 128r + 128)
+// and B columns [128r, 128r + 128) of the tile; one 256 x 256 x 16 MMA issued by the even CTA
+// reads both halves, and each CTA's TMEM holds its 128 rows x 256 columns.  A stage is 32 KiB
+// per CTA, so six stages fit beside the same epilogue staging.
+constexpr int kPairBM = 2 * kBM;                                  // 256 rows per pair tile
+constexpr int kPairBNHalf = kBN / 2;                              // B columns one CTA loads
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairBBytes = kBK * kPairBNHalf * kElemBytes;  // 16 KiB
+constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;       // 32 KiB per CTA
+constexpr uint32_t kPairTxBytes = 2 * kPairStageBytes;            // both CTAs' bytes, one barrier
+constexpr uint32_t kPairSmemBytes =
+    kSmemAlignSlack + kPairStages * kPairStageBytes + kEpiWarps * 2 * kEpiBufBytes;
+static_assert(kPairSmemBytes + 256 <= 232448, "shared memory per CTA (pair variant)");
+static_assert(kPairBNHalf % kBChunkCols == 0, "pair B half must be whole 64-column chunks");
+
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;
 constexpr uint32_t kRoleMma = 2u;

@@ -2,6 +2,7 @@
 // the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
 // tile-schedule inspection kernel, and the zero fill used when K == 0.
 #include "tg_gemm_kernel.cuh"
+#include "tg_gemm_pair_kernel.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -39,8 +40,7 @@ __global__ void zero_fill_kernel(uint4* __restrict__ dst, uint64_t n16) {
     dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int DT, bool DEBUG>
-cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
+GemmParams params_of(const GemmLaunch& l) {
   GemmParams p;
   p.M = l.M;
   p.N = l.N;
@@ -52,29 +52,67 @@ cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
   p.inject_skip_phase = l.inject_skip_phase;
-  gemm_persistent_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kSmemBytes, stream>>>(l.tmA, l.tmB,
-                                                                                 l.tmC, p);
+  return p;
+}
+
+template <int DT, bool DEBUG>
+cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
+  gemm_persistent_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kSmemBytes, stream>>>(
+      l.tmA, l.tmB, l.tmC, params_of(l));
+  return cudaGetLastError();
+}
+
+template <int DT, bool DEBUG>
+cudaError_t launch_pair(const GemmLaunch& l, cudaStream_t stream) {
+  gemm_pair_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kPairSmemBytes, stream>>>(
+      l.tmA, l.tmB, l.tmC, params_of(l));
   return cudaGetLastError();
 }
 
 template <int DT, bool DEBUG>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_persistent_ws_kernel<DT, DEBUG>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_persistent_ws_kernel<DT, DEBUG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_pair_ws_kernel<DT, DEBUG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
+                              static_cast<int>(kPairSmemBytes));
 }
 
 }  // namespace
 
-cudaError_t prepare_gemm_kernels() {
+cudaError_t prepare_gemm_kernels(int* max_pairs) {
   cudaError_t e;
   if ((e = set_smem_attr<0, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<1, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<0, true>()) != cudaSuccess) return e;
-  return set_smem_attr<1, true>();
+  if ((e = set_smem_attr<1, true>()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_ws_kernel<1, false>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pairs = clusters;
+  return cudaSuccess;
 }
 
-cudaError_t launch_gemm(int dtype, bool debug, const GemmLaunch& l, cudaStream_t stream) {
+cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
+                        cudaStream_t stream) {
+  if (variant == kVariantPair) {
+    if (dtype == 0)
+      return debug ? launch_pair<0, true>(l, stream) : launch_pair<0, false>(l, stream);
+    return debug ? launch_pair<1, true>(l, stream) : launch_pair<1, false>(l, stream);
+  }
   if (dtype == 0) return debug ? launch_one<0, true>(l, stream) : launch_one<0, false>(l, stream);
   return debug ? launch_one<1, true>(l, stream) : launch_one<1, false>(l, stream);
 }

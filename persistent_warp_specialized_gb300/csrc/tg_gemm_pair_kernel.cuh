@@ -1,0 +1,298 @@
+// tg_gemm_pair_kernel.cuh -- the CTA-pair (tcgen05 cta_group::2) persistent GEMM.
+//
+// "[Feature] Introduce tile scheduler #2441", gemm_tcgen5mma_ws_persistent.py,
+// ``gemm_persistent_2cta``: a cluster of two CTAs (``cluster_dims=2``) shares one 256 x 256
+// output tile.  Each CTA loads its own 128-row slice of A and its own half of B's columns
+// (``(by * 2 + cta_id) * block_N // 2``); only the even CTA issues the MMA
+// (``use_2cta=True``), arrivals on ``loaded`` and ``tmem_empty`` go to the even CTA's
+// barriers (``mbarrier_arrive(..., 0)``), and the MMA completions are signalled to both CTAs
+// (``arrive_2cta=True``).  The scheduler runs per cluster (``init(block_id // cluster_size)``)
+// over ceil(M / 256) x ceil(N / 256) pair tiles, and CTA r works on rows 256 * m_idx + 128 r
+// (the page's ``bx = m_idx * cluster_size + cta_id``).  When M is not a multiple of 256 the
+// odd CTA's slice of the last pair row lies partly or wholly past M: its TMA loads read zeros
+// there and its stores are clipped or skipped, so nothing outside A or C is touched (the
+// out-of-bounds ``bx`` the review of the PR warns about).
+//
+// Per CTA and k-block: A box 128 x 64 (16 KiB) and two B boxes 64 x 64 (16 KiB) into the
+// CTA's own ring slot; both CTAs' bytes complete on the even CTA's ``loaded[s]``, which the
+// even CTA arms with 64 KiB.  The MMA (M = 256, N = 256, K = 16, four per k-block) reads A
+// rows 0..127 and B columns 0..127 from the even CTA's slot and the rest from the odd
+// CTA's slot at the same offset, and writes 128 rows into each CTA's TMEM.  tcgen05.commit
+// with a CTA mask of 0b11 completes ``consumed[s]`` and ``tmem_full[w & 1]`` in both CTAs.
+// Both CTAs' epilogues arrive on the even CTA's ``tmem_empty[w & 1]`` (count 256).
+//
+// All tcgen05 instructions of this kernel use cta_group::2.  Waits are bounded exactly as in
+// the single-CTA kernel; an abort also raises the peer CTA's flag, and the pair meets at a
+// cluster barrier before TMEM is freed, so neither CTA leaves while the other may still
+// read its shared memory or write its TMEM.  Included by exactly one translation unit, after
+// tg_gemm_kernel.cuh.
+#pragma once
+
+#include "tg_gemm_kernel.cuh"
+
+namespace tg {
+
+struct __align__(8) PairCtl {
+  uint64_t loaded[kPairStages];      // used in the even CTA only
+  uint64_t consumed[kPairStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];            // used in the even CTA only (count 256)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Like wait_or_abort, but a timeout also raises the peer CTA's abort flag.
+__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag,
+                                                   uint32_t peer_abort_addr, uint64_t limit_ns,
+                                                   uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      st_shared_cluster_u32(peer_abort_addr, 1u);
+      atomicOr(&g_watchdog_status, role);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
+// DT: 0 = fp16, 1 = bf16.  p.m_blocks counts 256-row pair tiles, p.n_blocks 256-column tiles.
+template <int DT, bool DEBUG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PairCtl ctl;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = cluster_ctarank();          // 0: even CTA (issues the MMA), 1: odd
+  const uint32_t pair = blockIdx.x >> 1;
+  const uint32_t num_pairs = gridDim.x >> 1;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA0 = sbase;                        // A of stage s: sA0 + s * kPairStageBytes
+  const uint32_t sB0 = sbase + kABytes;              // B of stage s: sB0 + s * kPairStageBytes
+  const uint32_t sEpi = sbase + kPairStages * kPairStageBytes;
+
+  const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
+  const uint32_t bar_consumed = smem_u32(&ctl.consumed[0]);
+  const uint32_t bar_tmem_full = smem_u32(&ctl.tmem_full[0]);
+  const uint32_t bar_tmem_empty = smem_u32(&ctl.tmem_empty[0]);
+  const uint32_t bar_drain = smem_u32(&ctl.drain);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(bar_loaded + 8u * s, 1);
+      mbar_init(bar_consumed + 8u * s, 1);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tmem_full + 8u * b, 1);
+      mbar_init(bar_tmem_empty + 8u * b, 2 * kEpiThreads);
+    }
+    mbar_init(bar_drain, 1);
+    ctl.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  __syncwarp();
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tcgen05_fence_before_sync();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrive or complete_tx
+  tcgen05_fence_after_sync();
+
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&ctl.abort), rank ^ 1u);
+  const uint64_t limit = p.watchdog_ns;
+  const uint64_t k_blocks = p.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+      sched.init(pair);
+      uint32_t pending = 0, pending_par = 0;
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint64_t w = sched.current_iter;
+        const int32_t m0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM);
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx * kBN + rank * kPairBNHalf);
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = w * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kPairStages) & 1u);
+          if (!pair_wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, peer_abort, limit,
+                                  kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          pending &= ~(1u << s);
+          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
+          if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, kPairTxBytes);
+          const int32_t kx = static_cast<int32_t>(k) * kBK;
+          tma_load_2d_pair(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0);
+#pragma unroll
+          for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c)
+            tma_load_2d_pair(sB0 + s * kPairStageBytes + c * kBChunkBytes, &tmB, full_even,
+                             n0 + static_cast<int32_t>(c * kBChunkCols), kx);
+          pending |= 1u << s;
+          pending_par = (pending_par & ~(1u << s)) | (par << s);
+        }
+        sched.next_tile();
+      }
+      if (!ok) {
+        if (rank == 0) {
+          for (uint32_t s = 0; s < kPairStages; ++s)
+            if ((pending >> s) & 1u)
+              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+        } else if (pending) {
+          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
+          // give them time to land before this CTA may leave
+          spin_ns(limit < 1000000ull ? limit : 1000000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+      sched.init(pair);
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint32_t w = sched.current_iter;
+        const uint32_t buf = w & 1u;
+        if (!pair_wait_or_abort(bar_tmem_empty + 8u * buf, ((w >> 1) & 1u) ^ 1u, abort_flag,
+                                peer_abort, limit, kRoleMma)) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * kBN;
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kPairStages) & 1u);
+          if (!pair_wait_or_abort(bar_loaded + 8u * s, par, abort_flag, peer_abort, limit,
+                                  kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after_sync();
+          const uint32_t a_addr = sA0 + s * kPairStageBytes;
+          const uint32_t b_addr = sB0 + s * kPairStageBytes;
+#pragma unroll
+          for (uint32_t kk = 0; kk < kBK / kUmmaK; ++kk) {
+            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kBChunkBytes, 1024);
+            umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(bar_tmem_full + 8u * buf, 0x3);
+        sched.next_tile();
+      }
+      umma_commit_pair_multicast(bar_drain, 0x1);
+      wait_bounded(bar_drain, 0, limit, kRoleDrain);
+    }
+    __syncwarp();
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const uint32_t q = warp - kFirstEpiWarp;
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+    sched.init(pair);
+    uint32_t chunk = 0;
+    while (sched.valid()) {
+      const uint32_t w = sched.current_iter;
+      const uint32_t buf = w & 1u;
+      const bool got = pair_wait_or_abort(bar_tmem_full + 8u * buf, (w >> 1) & 1u, abort_flag,
+                                          peer_abort, limit, kRoleEpilogue);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tcgen05_fence_after_sync();
+      const int32_t row0 =
+          static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM + q * 32u);
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN;
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kBN;
+#pragma unroll 1
+      for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+        uint32_t v[64];
+        tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
+        if (j == kBN / kEpiN - 1) {
+          tcgen05_fence_before_sync();
+          mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * buf, 0));
+        }
+        const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t row_addr = sbuf + lane * 128u;
+#pragma unroll
+        for (uint32_t c = 0; c < 8; ++c) {
+          st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4),
+                       pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
+                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
+                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
+                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t x = col0 + static_cast<int32_t>(j * kEpiN);
+          if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
+            tma_store_2d(&tmC, sbuf, x, row0);
+          bulk_commit_group();
+        }
+        __syncwarp();
+      }
+      if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
+        int32_t* tr = p.trace + 4ull * sched.linear_idx;
+        tr[0] = static_cast<int32_t>(pair);
+        tr[1] = static_cast<int32_t>(w);
+        tr[2] = static_cast<int32_t>(sched.m_idx);
+        tr[3] = static_cast<int32_t>(sched.n_idx);
+      }
+      sched.next_tile();
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tcgen05_fence_before_sync();
+  cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
+  if (warp == 2) {
+    tcgen05_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tg

@@ -19,10 +19,16 @@ struct GemmLaunch {
   int64_t inject_skip_phase;
 };
 
-// Sets the dynamic shared-memory limit of every GEMM instantiation on the current device.
-cudaError_t prepare_gemm_kernels();
-// dtype 0 = fp16, 1 = bf16
-cudaError_t launch_gemm(int dtype, bool debug, const GemmLaunch& l, cudaStream_t stream);
+// kernel variants: one CTA per 128 x 256 tile, or a CTA pair (cta_group::2) per 256 x 256 tile
+enum Variant { kVariantSingle = 1, kVariantPair = 2 };
+
+// Sets the dynamic shared-memory limit of every GEMM instantiation on the current device and
+// returns how many CTA pairs of the pair kernel can be resident at once (*max_pairs).
+cudaError_t prepare_gemm_kernels(int* max_pairs);
+// dtype 0 = fp16, 1 = bf16.  For the pair variant l.grid counts CTAs (even) and l.m_blocks
+// counts 256-row pair tiles.
+cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
+                        cudaStream_t stream);
 // C[0 .. bytes) = 0 (bytes a multiple of 16, C 16-byte aligned)
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream);
 cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
