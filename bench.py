@@ -165,25 +165,36 @@ class ClockSampler:
         lines = self.out.read().strip().splitlines()
         self.out.close()
         os.unlink(self.out.name)
-        rows = []
-        for line in lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
-            except ValueError:
-                continue
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
-        if not inside:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[1] for r in inside),
-                "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside)}
+        return parse_clock_csv(lines, t0, t1)
+
+
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_clock_csv(lines, t0, t1):
+    """Summarise nvidia-smi rows (ClockSampler.FIELDS, csv, no header, no units) whose
+    timestamp lies in [t0, t1] (host epoch seconds): median and max SM clock, and every
+    throttle reason seen active."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            stamp, frac = (parts[0].split(".") + ["0"])[:2]
+            ts = time.mktime(time.strptime(stamp, "%Y/%m/%d %H:%M:%S")) + float("0." + frac)
+            rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+        except ValueError:
+            continue
+    inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": max((r[2] for r in rows), default=None),
+                "reasons": [], "samples": 0}
+    reasons = sorted({CLOCK_REASONS[i] for r in inside for i, v in enumerate(r[3])
+                      if v.lower() == "active"})
+    return {"sm_mhz": statistics.median(r[1] for r in inside),
+            "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+            "samples": len(inside)}
 
 
 def profile_traffic():
