@@ -101,6 +101,18 @@ const char* tg_last_error(void);
 int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* group);
 
 /*
+ * tg_gemm_launch_shape -- the persistent launch the library would use for an M x N x K
+ * problem on the current device with ``variant`` (TG_VARIANT_*; AUTO is resolved).
+ *   *variant_out: the concrete variant; *tile_m, *tile_n: the output tile of one scheduler
+ *   worker; *m_tiles, *n_tiles: the tile grid; *workers: scheduler workers (CTAs for SINGLE,
+ *   CTA pairs for PAIR); *ctas: CTAs launched.  Any pointer may be NULL.
+ * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
+ */
+int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
+                         int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
+                         int* ctas);
+
+/*
  * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
  *   variant: TG_VARIANT_* as in tg_gemm_persistent_ex.
  *   trace_dev: NULL or a device buffer of 4 int32 per output tile of the variant (128 x 256

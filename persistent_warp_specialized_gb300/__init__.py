@@ -35,6 +35,7 @@ EXPORTED = (
     "tg_tile_schedule",
     "tg_last_error",
     "tg_gemm_config",
+    "tg_gemm_launch_shape",
     "tg_gemm_persistent_debug",
     "tg_device_status",
     "tg_gemm_persistent_host",
@@ -71,6 +72,8 @@ def load_library(path=LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
     lib.tg_gemm_config.restype = i32
+    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32, ip, ip, ip, ip, ip, ip, ip]
+    lib.tg_gemm_launch_shape.restype = i32
     lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
                                              i64]
     lib.tg_gemm_persistent_debug.restype = i32
@@ -156,6 +159,15 @@ def tg_gemm_config():
     vals = [ctypes.c_int() for _ in range(5)]
     _check(load_library().tg_gemm_config(*[ctypes.byref(v) for v in vals]))
     keys = ("block_m", "block_n", "block_k", "stages", "group")
+    return dict(zip(keys, (v.value for v in vals)))
+
+
+def tg_gemm_launch_shape(M, N, K, variant="auto"):
+    """The persistent launch the library uses for M x N x K on the current device."""
+    vals = [ctypes.c_int() for _ in range(7)]
+    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant),
+                                               *[ctypes.byref(v) for v in vals]))
+    keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas")
     return dict(zip(keys, (v.value for v in vals)))
 
 

@@ -175,6 +175,25 @@ int auto_variant(int64_t /*M*/, int64_t /*N*/, int64_t /*K*/, int max_pairs) {
   return TG_VARIANT_SINGLE;
 }
 
+struct Shape {
+  uint32_t tile_m, tile_n, m_tiles, n_tiles, workers, ctas;
+};
+
+// Persistent launch of a concrete variant: one worker per SM (SINGLE) or per resident CTA
+// pair (PAIR), never more workers than tiles.
+Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, int sms, int max_pairs) {
+  Shape sh;
+  sh.tile_m = variant == TG_VARIANT_PAIR ? tg::kPairBM : tg::kBM;
+  sh.tile_n = tg::kBN;
+  sh.m_tiles = static_cast<uint32_t>((M + sh.tile_m - 1) / sh.tile_m);
+  sh.n_tiles = static_cast<uint32_t>((N + sh.tile_n - 1) / sh.tile_n);
+  const uint64_t tiles = uint64_t(sh.m_tiles) * sh.n_tiles;
+  const uint64_t slots = variant == TG_VARIANT_PAIR ? uint64_t(max_pairs) : uint64_t(sms);
+  sh.workers = static_cast<uint32_t>(tiles < slots ? tiles : slots);
+  sh.ctas = variant == TG_VARIANT_PAIR ? 2 * sh.workers : sh.workers;
+  return sh;
+}
+
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
               void* stream, int variant, bool debug, int32_t* trace, uint64_t watchdog_ns,
               int64_t inject) {
@@ -200,18 +219,12 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
-  const int64_t tile_m = variant == TG_VARIANT_PAIR ? tg::kPairBM : tg::kBM;
-  l.m_blocks = static_cast<uint32_t>((M + tile_m - 1) / tile_m);
-  l.n_blocks = static_cast<uint32_t>((N + tg::kBN - 1) / tg::kBN);
+  const Shape sh = launch_shape(M, N, K, variant, sms, max_pairs);
+  l.m_blocks = sh.m_tiles;
+  l.n_blocks = sh.n_tiles;
   l.k_blocks = static_cast<uint32_t>((K + tg::kBK - 1) / tg::kBK);
   l.group = tg::kGroup;
-  const uint64_t tiles = uint64_t(l.m_blocks) * l.n_blocks;
-  if (variant == TG_VARIANT_PAIR) {
-    const uint64_t pairs = tiles < uint64_t(max_pairs) ? tiles : uint64_t(max_pairs);
-    l.grid = static_cast<uint32_t>(2 * pairs);
-  } else {
-    l.grid = static_cast<uint32_t>(tiles < uint64_t(sms) ? tiles : uint64_t(sms));
-  }
+  l.grid = sh.ctas;
   l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
   l.trace = trace;
   l.inject_skip_phase = inject;
@@ -244,6 +257,28 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev, int64_
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
                           int64_t N, int64_t K, int dtype, void* stream, int variant) {
   return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, false, nullptr, 0, -1);
+}
+
+int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
+                         int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
+                         int* ctas) {
+  if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
+    return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
+  int sms = 0, max_pairs = 0;
+  int rc = device_ready(&sms, &max_pairs);
+  if (rc != TG_OK) return rc;
+  if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, sms, max_pairs);
+  if (variant_out) *variant_out = variant;
+  if (tile_m) *tile_m = static_cast<int>(sh.tile_m);
+  if (tile_n) *tile_n = static_cast<int>(sh.tile_n);
+  if (m_tiles) *m_tiles = static_cast<int>(sh.m_tiles);
+  if (n_tiles) *n_tiles = static_cast<int>(sh.n_tiles);
+  if (workers) *workers = static_cast<int>(sh.workers);
+  if (ctas) *ctas = static_cast<int>(sh.ctas);
+  return TG_OK;
 }
 
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,

@@ -66,3 +66,27 @@ def ulp_diff_stats(c_bits, ref_bits, dtype):
     u = formats.ulp(ref_bits, dtype)
     d = np.abs(c - r) / u
     return int((d > 1.0).sum()), float(d.max())
+
+
+def assert_within_accumulation_bound(c_bits, ref_bits, a_cpu, b_cpu, dtype, what=""):
+    """A bound tighter than the acceptance gate, from the arithmetic of the kernel.
+
+    The kernel sums K exact products in fp32 and rounds once to the output type; the oracle
+    rounds the exact sum once.  With S = |A|.|B| (binary64) and the fp32 summation bound
+    gamma_K = K u / (1 - K u), u = 2^-23 (one unit of fp32 roundoff, allowing the tensor
+    core to truncate rather than round), every element must satisfy
+        |C - C_ref| <= 2 ulp(C_ref) + gamma_K S.
+    Near-zero outputs with heavy cancellation may be many output ulps off and still inside it.
+    """
+    a = formats.decode(wl.bits(a_cpu), dtype)
+    b = formats.decode(wl.bits(b_cpu), dtype)
+    s = np.abs(a) @ np.abs(b)
+    K = a.shape[1]
+    u = 2.0 ** -23
+    gamma = K * u / (1 - K * u)
+    c = formats.decode(c_bits, dtype)
+    r = formats.decode(ref_bits, dtype)
+    bound = 2.0 * formats.ulp(ref_bits, dtype) + gamma * s
+    bad = np.abs(c - r) > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside the fp32 accumulation "
+                           f"bound; first at {np.argwhere(bad)[:4].tolist()}")
