@@ -21,9 +21,19 @@
 namespace tg {
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;
+#ifndef TG_BN
+#define TG_BN 256
+#endif
+constexpr int kBN = TG_BN;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+// Ring depths can be overridden at compile time (-DTG_STAGES=, -DTG_PAIR_STAGES=) to tune.
+#ifndef TG_STAGES
+#define TG_STAGES 4
+#endif
+#ifndef TG_PAIR_STAGES
+#define TG_PAIR_STAGES 6
+#endif
+constexpr int kStages = TG_STAGES;
 constexpr int kEpiN = 64;
 constexpr int kGroup = 8;
 constexpr int kThreads = 256;
@@ -58,7 +68,7 @@ static_assert(kSmemBytes + 256 <= 232448, "shared memory per CTA");
 // per CTA, so six stages fit beside the same epilogue staging.
 constexpr int kPairBM = 2 * kBM;                                  // 256 rows per pair tile
 constexpr int kPairBNHalf = kBN / 2;                              // B columns one CTA loads
-constexpr int kPairStages = 6;
+constexpr int kPairStages = TG_PAIR_STAGES;
 constexpr uint32_t kPairBBytes = kBK * kPairBNHalf * kElemBytes;  // 16 KiB
 constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;       // 32 KiB per CTA
 constexpr uint32_t kPairTxBytes = 2 * kPairStageBytes;            // both CTAs' bytes, one barrier
