@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
     ap.add_argument("--workload", default="gemm_8192_bf16")
+    ap.add_argument("--variant", choices=["auto", "single", "pair"], default="auto",
+                    help="kernel variant (auto: the library's choice, as tg_gemm_persistent)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
@@ -277,7 +279,7 @@ def workload_config(w):
             "accumulate": "fp32", "inputs": f"{w.dist}, seed {w.seed}",
             "l2": "inputs larger than L2 (no flush)" if 2 * (w.M * w.K + w.K * w.N) > 129e6
                   else "inputs fit in L2 (no flush; warm L2)",
-            "tile": "128x256x64, 4 stages, persistent grid = #SMs"}
+            "tile": "block_K 64; persistent: one scheduler worker per SM (single) or SM pair (pair)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -306,8 +308,12 @@ def run_tg(args):
     stream = torch.cuda.current_stream(dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    def step():
-        tg.tg_gemm_persistent(a, b, c, w.M, w.N, w.K, w.dtype, stream)
+    if args.variant == "auto":
+        def step():
+            tg.tg_gemm_persistent(a, b, c, w.M, w.N, w.K, w.dtype, stream)
+    else:
+        def step():
+            tg.tg_gemm_persistent_ex(a, b, c, w.M, w.N, w.K, w.dtype, stream, args.variant)
 
     steps, warm = max(1, args.steps), max(3, args.warmup)
     for _ in range(warm):
@@ -382,7 +388,8 @@ def run_tg(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see config.inputs)",
-        "config": dict(workload_config(w), sms=sms, grid=min(sms, -(-w.M // 128) * -(-w.N // 256))),
+        "config": dict(workload_config(w), sms=sms,
+                       launch=tg.tg_gemm_launch_shape(w.M, w.N, w.K, args.variant)),
         "gpu_launches": steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
     }
 

@@ -42,9 +42,11 @@ def _inputs():
 
 
 def _stamp():
+    """sha256 of the library's sources (by path relative to the repository) and flags: the
+    same on every machine for the same sources."""
     h = hashlib.sha256()
     for path in _inputs():
-        h.update(path.encode())
+        h.update(os.path.relpath(path, ROOT).encode())
         with open(path, "rb") as f:
             h.update(f.read())
     h.update(" ".join(FLAGS).encode())

@@ -26,14 +26,23 @@ def nan_filled(M, N, dtype):
     return c
 
 
-def run_gpu(a_cpu, b_cpu, dtype, stream=None):
-    """C bits (numpy uint16) from tg_gemm_persistent on device copies of a_cpu, b_cpu."""
+# the kernel variants every parity test runs; "auto" is what tg_gemm_persistent (and the
+# benchmark) runs
+VARIANTS = ["single", "pair"]
+
+
+def run_gpu(a_cpu, b_cpu, dtype, stream=None, variant=None):
+    """C bits (numpy uint16) from the GEMM on device copies of a_cpu, b_cpu: through
+    tg_gemm_persistent when ``variant`` is None, else tg_gemm_persistent_ex(variant)."""
     M, K = a_cpu.shape
     N = b_cpu.shape[1]
     a = a_cpu.cuda()
     b = b_cpu.cuda()
     c = nan_filled(M, N, dtype)
-    tg.tg_gemm_persistent(a, b, c, M, N, K, dtype, stream)
+    if variant is None:
+        tg.tg_gemm_persistent(a, b, c, M, N, K, dtype, stream)
+    else:
+        tg.tg_gemm_persistent_ex(a, b, c, M, N, K, dtype, stream, variant)
     torch.cuda.synchronize()
     assert tg.tg_device_status() == 0
     return wl.bits(c.cpu())

@@ -14,7 +14,7 @@ import persistent_warp_specialized_gb300 as tg
 from persistent_warp_specialized_gb300 import workloads as wl
 from oracle import formats
 
-from gpu_helpers import assert_within_tolerance, ensure_library, oracle_bits, run_gpu
+from gpu_helpers import VARIANTS, assert_within_tolerance, ensure_library, oracle_bits, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -36,53 +36,60 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("shape", SHAPES)
-def test_small_shapes_match_oracle(shape, dtype):
+def test_small_shapes_match_oracle(shape, dtype, variant):
     M, N, K = shape
     a, b = wl.make_inputs(M, N, K, dtype, "uniform", seed=M + N + K)
-    assert_within_tolerance(run_gpu(a, b, dtype), oracle_bits(a, b, dtype), dtype, str(shape))
+    assert_within_tolerance(run_gpu(a, b, dtype, variant=variant), oracle_bits(a, b, dtype),
+                            dtype, f"{shape} {variant}")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype,K", [("f16", 512), ("bf16", 64), ("f16", 200), ("bf16", 40)])
-def test_integer_inputs_are_bit_exact(dtype, K):
+def test_integer_inputs_are_bit_exact(dtype, K, variant):
     # entries in [-2, 2]: |C| <= 4K, exact in the output type (f16: 2048, bf16: 256)
     M, N = 300, 776
     a, b = wl.small_int_inputs(M, N, K, dtype, seed=K)
-    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+    assert np.array_equal(run_gpu(a, b, dtype, variant=variant), oracle_bits(a, b, dtype))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_many_tiles_per_cta_with_short_k(dtype):
+def test_many_tiles_per_cta_with_short_k(dtype, variant):
     # 32 x 16 = 512 tiles (> 3 per SM); k_blocks = 3 is not a multiple of the 4 stages, the
     # case where indexing the consumer's slot by k instead of the phase goes wrong
     M, N, K = 4096, 4096, 192
     a, b = wl.small_int_inputs(M, N, K, dtype, lo=-1, hi=1, seed=9)
-    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+    assert np.array_equal(run_gpu(a, b, dtype, variant=variant), oracle_bits(a, b, dtype))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_k_shorter_than_one_block_many_tiles(dtype):
+def test_k_shorter_than_one_block_many_tiles(dtype, variant):
     M, N, K = 2048, 2048, 8          # k_blocks = 1: every phase is a new tile
     a, b = wl.small_int_inputs(M, N, K, dtype, seed=4)
-    assert np.array_equal(run_gpu(a, b, dtype), oracle_bits(a, b, dtype))
+    assert np.array_equal(run_gpu(a, b, dtype, variant=variant), oracle_bits(a, b, dtype))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_identity_reproduces_operand(dtype):
+def test_identity_reproduces_operand(dtype, variant):
     n = 384
     eye = torch.eye(n, dtype=wl.TORCH_DTYPES[dtype])
     x, _ = wl.make_inputs(n, 8, 520, dtype, "uniform", seed=2)      # [384, 520]
-    assert np.array_equal(run_gpu(eye, x, dtype), wl.bits(x))        # I . X = X
+    assert np.array_equal(run_gpu(eye, x, dtype, variant=variant), wl.bits(x))   # I . X = X
     y, _ = wl.make_inputs(300, 8, n, dtype, "uniform", seed=3)       # [300, 384]
-    assert np.array_equal(run_gpu(y, eye, dtype), wl.bits(y))        # Y . I = Y
+    assert np.array_equal(run_gpu(y, eye, dtype, variant=variant), wl.bits(y))   # Y . I = Y
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype,K", [("f16", 2048), ("bf16", 8192)])
-def test_all_ones_give_k(dtype, K):
-    M, N = 256, 512
+def test_all_ones_give_k(dtype, K, variant):
+    M, N = 384, 512
     t = wl.TORCH_DTYPES[dtype]
-    c = run_gpu(torch.ones((M, K), dtype=t), torch.ones((K, N), dtype=t), dtype)
+    c = run_gpu(torch.ones((M, K), dtype=t), torch.ones((K, N), dtype=t), dtype, variant=variant)
     assert np.array_equal(formats.decode(c, dtype), np.full((M, N), float(K)))
 
 

@@ -13,7 +13,7 @@ import persistent_warp_specialized_gb300 as tg
 from persistent_warp_specialized_gb300 import workloads as wl
 from oracle import schedule
 
-from gpu_helpers import assert_within_tolerance, ensure_library, oracle_bits
+from gpu_helpers import VARIANTS, assert_within_tolerance, ensure_library, oracle_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -51,31 +51,32 @@ def test_config1_schedule_148_workers():
         (0, 0, 0, 0), (1, 0, 1, 0)]
 
 
-@pytest.mark.parametrize("M,N,K", [(4000, 7000, 256), (8192, 8192, 64), (1024, 1024, 1024), (256, 256, 256)])
-def test_kernel_followed_the_schedule(M, N, K):
-    # the epilogue of the real GEMM records (cta, w, bx, by) for every tile it stored
-    cfg = tg.tg_gemm_config()
-    m_blocks = -(-M // cfg["block_m"])
-    n_blocks = -(-N // cfg["block_n"])
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    workers = min(sms, m_blocks * n_blocks)
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("M,N,K", [(4000, 7000, 256), (8192, 8192, 64), (1024, 1024, 1024),
+                                   (256, 256, 256), (4000, 2048, 128)])
+def test_kernel_followed_the_schedule(M, N, K, variant):
+    # the epilogue of the real GEMM records (worker, w, bx, by) for every tile it stored
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant)
+    m_tiles, n_tiles, workers = shape["m_tiles"], shape["n_tiles"], shape["workers"]
     a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=M)
     a_d, b_d = a.cuda(), b.cuda()
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    trace = torch.full((m_blocks * n_blocks, 4), -1, dtype=torch.int32, device="cuda")
-    assert tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", trace=trace) == 0
-    want = schedule.enumerate_schedule(m_blocks, n_blocks, workers, cfg["group"])
+    trace = torch.full((m_tiles * n_tiles, 4), -1, dtype=torch.int32, device="cuda")
+    assert tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
+                                       trace=trace) == 0
+    want = schedule.enumerate_schedule(m_tiles, n_tiles, workers, tg.tg_gemm_config()["group"])
     by_tile = {}
-    for (cta, w, bx, by) in want:
-        by_tile[cta + w * workers] = (cta, w, bx, by)
+    for (worker, w, bx, by) in want:
+        by_tile[worker + w * workers] = (worker, w, bx, by)
     got = trace.cpu().numpy()
-    for t in range(m_blocks * n_blocks):
+    for t in range(m_tiles * n_tiles):
         assert tuple(int(v) for v in got[t]) == by_tile[t], t
     # the debug build computes the same product
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "debug build")
 
 
-def test_watchdog_fires_and_context_survives():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_watchdog_fires_and_context_survives(variant):
     # CTA 0's producer never fills pipeline phase 5: the MMA role's wait on it cannot
     # complete, the 20 ms watchdog must end every role and report TG_ERR_TIMEOUT
     M, N, K = 512, 512, 1024
@@ -83,13 +84,13 @@ def test_watchdog_fires_and_context_survives():
     a_d, b_d = a.cuda(), b.cuda()
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tg.TgError) as e:
-        tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", watchdog_ns=20_000_000,
-                                    inject_skip_phase=5)
+        tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
+                                    watchdog_ns=20_000_000, inject_skip_phase=5)
     assert e.value.code == tg.TG_ERR_TIMEOUT
     assert "watchdog" in str(e.value)
     # the context is intact: the status word was cleared and the next GEMM is correct
     assert tg.tg_device_status() == 0
-    tg.tg_gemm_persistent(a_d, b_d, c, M, N, K, "bf16")
+    tg.tg_gemm_persistent_ex(a_d, b_d, c, M, N, K, "bf16", variant=variant)
     torch.cuda.synchronize()
     assert tg.tg_device_status() == 0
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "after watchdog")
