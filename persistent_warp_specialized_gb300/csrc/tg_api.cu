@@ -216,6 +216,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kBK, tg::kBM, "A")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, tg::kBK, "B")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
+  l.C = C;
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);

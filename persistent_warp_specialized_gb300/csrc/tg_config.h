@@ -33,7 +33,23 @@ constexpr int kBK = 64;
 #ifndef TG_PAIR_STAGES
 #define TG_PAIR_STAGES 6
 #endif
+// L2 policy of the A and B loads (0 none, 1 evict_first, 2 evict_last, 3 evict_normal)
+#ifndef TG_A_POLICY
+#define TG_A_POLICY 0
+#endif
+#ifndef TG_B_POLICY
+#define TG_B_POLICY 0
+#endif
+// Epilogue store path: 0 = through shared memory and TMA stores (the page's use_tma_store),
+// 1 = 16-byte stores straight from registers (the page's direct C_local_cast store), which
+// needs no staging buffers and leaves that shared memory to the operand ring.
+#ifndef TG_EPI_DIRECT
+#define TG_EPI_DIRECT 0
+#endif
 constexpr int kStages = TG_STAGES;
+constexpr int kAPolicy = TG_A_POLICY;
+constexpr int kBPolicy = TG_B_POLICY;
+constexpr bool kEpiDirect = TG_EPI_DIRECT != 0;
 constexpr int kEpiN = 64;
 constexpr int kGroup = 8;
 constexpr int kThreads = 256;
@@ -50,8 +66,8 @@ constexpr uint32_t kBChunkCols = 64;                             // one 128-byte
 constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * kElemBytes;  // 8 KiB
 constexpr uint32_t kEpiBufBytes = 32 * kEpiN * kElemBytes;       // 4 KiB: 32 rows x 128 bytes
 constexpr uint32_t kSmemAlignSlack = 1024;
-constexpr uint32_t kSmemBytes =
-    kSmemAlignSlack + kStages * kStageBytes + kEpiWarps * 2 * kEpiBufBytes;
+constexpr uint32_t kEpiSmemBytes = kEpiDirect ? 0u : kEpiWarps * 2 * kEpiBufBytes;
+constexpr uint32_t kSmemBytes = kSmemAlignSlack + kStages * kStageBytes + kEpiSmemBytes;
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kBK * kElemBytes == 128, "block_K must span one 128-byte swizzle row");
@@ -72,8 +88,7 @@ constexpr int kPairStages = TG_PAIR_STAGES;
 constexpr uint32_t kPairBBytes = kBK * kPairBNHalf * kElemBytes;  // 16 KiB
 constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;       // 32 KiB per CTA
 constexpr uint32_t kPairTxBytes = 2 * kPairStageBytes;            // both CTAs' bytes, one barrier
-constexpr uint32_t kPairSmemBytes =
-    kSmemAlignSlack + kPairStages * kPairStageBytes + kEpiWarps * 2 * kEpiBufBytes;
+constexpr uint32_t kPairSmemBytes = kSmemAlignSlack + kPairStages * kPairStageBytes + kEpiSmemBytes;
 static_assert(kPairSmemBytes + 256 <= 232448, "shared memory per CTA (pair variant)");
 static_assert(kPairBNHalf % kBChunkCols == 0, "pair B half must be whole 64-column chunks");
 

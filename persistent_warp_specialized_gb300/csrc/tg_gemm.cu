@@ -42,6 +42,7 @@ __global__ void zero_fill_kernel(uint4* __restrict__ dst, uint64_t n16) {
 
 GemmParams params_of(const GemmLaunch& l) {
   GemmParams p;
+  p.C = l.C;
   p.M = l.M;
   p.N = l.N;
   p.K = l.K;

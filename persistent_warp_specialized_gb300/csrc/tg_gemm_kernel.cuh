@@ -48,6 +48,7 @@
 namespace tg {
 
 struct GemmParams {
+  void* C;                     // output base (used by the direct-store epilogue)
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint64_t watchdog_ns;
@@ -117,6 +118,65 @@ __device__ __forceinline__ uint32_t pack_out(uint32_t lo_bits, uint32_t hi_bits)
   }
 }
 
+// Stores this warp's 32 rows x 64 columns of the accumulator (v: lane = row, 64 columns),
+// converted to the output type, at rows row0 .. row0 + 31 and columns x .. x + 63 of C.
+// Rows >= M and columns >= N are not written.
+//  * staged (default): each lane writes its row as eight 16-byte chunks into a 128-byte
+//    swizzled staging buffer (chunk c of row r at chunk c ^ (r % 8): conflict-free), the
+//    warp fences the writes into the async proxy, and lane 0 issues one TMA store, which
+//    clips at the tensor's edge.  Two buffers per warp alternate; before one is rewritten,
+//    lane 0 waits until the store that read it is done.  One bulk group per chunk.
+//  * direct: each lane stores its row's 128 bytes with 16-byte stores.
+template <int DT>
+__device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], uint32_t lane,
+                                                     uint32_t sbuf, const CUtensorMap* tmC,
+                                                     const GemmParams& p, int32_t row0,
+                                                     int32_t x) {
+  if constexpr (kEpiDirect) {
+    const int32_t row = row0 + static_cast<int32_t>(lane);
+    if (row < static_cast<int32_t>(p.M)) {
+      char* base = static_cast<char*>(p.C) +
+                   (static_cast<uint64_t>(row) * p.N + static_cast<uint64_t>(x)) * kElemBytes;
+#pragma unroll
+      for (uint32_t c = 0; c < 8; ++c) {
+        if (x + static_cast<int32_t>(8 * c) < static_cast<int32_t>(p.N))
+          st_global_v4(base + 16 * c, pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
+                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
+                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
+                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
+      }
+    }
+  } else {
+    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read sbuf is done
+    __syncwarp();
+    const uint32_t row_addr = sbuf + lane * 128u;
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) {
+      st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4), pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
+                   pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
+                   pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
+                   pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
+        tma_store_2d(tmC, sbuf, x, row0);
+      bulk_commit_group();   // one group per chunk, empty when the chunk is outside C
+    }
+  }
+  __syncwarp();   // converged for the next warp-collective tcgen05.ld
+}
+
+// A and B loads of one k-block slot, with the configured L2 policies.
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int32_t x, int32_t y, uint64_t policy, int kind) {
+  if (kind != 0)
+    tma_load_2d_hint(dst, map, bar, x, y, policy);
+  else
+    tma_load_2d(dst, map, bar, x, y);
+}
+
 // DT: 0 = fp16, 1 = bf16 (input and output).  DEBUG adds the tile trace and fault injection.
 template <int DT, bool DEBUG>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -178,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
       sched.init(blockIdx.x);
+      const uint64_t pol_a = l2_policy<kAPolicy>();
+      const uint64_t pol_b = l2_policy<kBPolicy>();
       uint32_t pending = 0;       // stages whose latest fill may still be in flight
       uint32_t pending_par = 0;   // parity of that fill, one bit per stage
       bool ok = true;
@@ -199,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = bar_loaded + 8u * s;
           mbar_arrive_expect_tx(full, kStageBytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
-          tma_load_2d(sA0 + s * kStageBytes, &tmA, full, kx, m0);
+          load_operand(sA0 + s * kStageBytes, &tmA, full, kx, m0, pol_a, kAPolicy);
 #pragma unroll
           for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
-            tma_load_2d(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
-                        n0 + static_cast<int32_t>(c * kBChunkCols), kx);
+            load_operand(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
+                         n0 + static_cast<int32_t>(c * kBChunkCols), kx, pol_b, kBPolicy);
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);
         }
@@ -291,26 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar_tmem_empty + 8u * buf);
         }
         const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
-        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read sbuf is done
-        __syncwarp();
-        const uint32_t row_addr = sbuf + lane * 128u;
-#pragma unroll
-        for (uint32_t c = 0; c < 8; ++c) {
-          st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4),
-                       pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
-                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
-                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
-                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          const int32_t x = col0 + static_cast<int32_t>(j * kEpiN);
-          if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
-            tma_store_2d(&tmC, sbuf, x, row0);
-          bulk_commit_group();   // one group per chunk, empty when the chunk is outside C
-        }
-        __syncwarp();   // converged for the next warp-collective tcgen05.ld
+        epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
+                                 col0 + static_cast<int32_t>(j * kEpiN));
       }
       if (DEBUG && p.trace != nullptr && q == 0 && lane == 0) {
         int32_t* tr = p.trace + 4ull * sched.linear_idx;

@@ -138,6 +138,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
       sched.init(pair);
+      const uint64_t pol_a = l2_policy<kAPolicy>();
+      const uint64_t pol_b = l2_policy<kBPolicy>();
       uint32_t pending = 0, pending_par = 0;
       bool ok = true;
       while (ok && sched.valid()) {
@@ -159,11 +161,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, kPairTxBytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
-          tma_load_2d_pair(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0);
+          if (kAPolicy != 0)
+            tma_load_2d_pair_hint(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0, pol_a);
+          else
+            tma_load_2d_pair(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0);
 #pragma unroll
-          for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c)
-            tma_load_2d_pair(sB0 + s * kPairStageBytes + c * kBChunkBytes, &tmB, full_even,
-                             n0 + static_cast<int32_t>(c * kBChunkCols), kx);
+          for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c) {
+            const uint32_t dst = sB0 + s * kPairStageBytes + c * kBChunkBytes;
+            const int32_t nx = n0 + static_cast<int32_t>(c * kBChunkCols);
+            if (kBPolicy != 0)
+              tma_load_2d_pair_hint(dst, &tmB, full_even, nx, kx, pol_b);
+            else
+              tma_load_2d_pair(dst, &tmB, full_even, nx, kx);
+          }
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);
         }
@@ -253,26 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * buf, 0));
         }
         const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-        const uint32_t row_addr = sbuf + lane * 128u;
-#pragma unroll
-        for (uint32_t c = 0; c < 8; ++c) {
-          st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4),
-                       pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
-                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
-                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
-                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          const int32_t x = col0 + static_cast<int32_t>(j * kEpiN);
-          if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
-            tma_store_2d(&tmC, sbuf, x, row0);
-          bulk_commit_group();
-        }
-        __syncwarp();
+        epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
+                                 col0 + static_cast<int32_t>(j * kEpiN));
       }
       if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
         int32_t* tr = p.trace + 4ull * sched.linear_idx;

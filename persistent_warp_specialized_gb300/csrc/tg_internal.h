@@ -11,6 +11,7 @@ namespace tg {
 
 struct GemmLaunch {
   CUtensorMap tmA, tmB, tmC;
+  void* C;
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t grid;
