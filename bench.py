@@ -41,7 +41,8 @@ UNIT = "TFLOP/s"
 NOMINAL_DENSE_BF16_TFLOPS = 2250.0       # GB300 dense bf16/fp16, no sparsity
 DENSE_FLOP_PER_CLK_PER_SM = 8192         # derived: one 128x256x16 MMA per 128 cycles
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_persistent_ws_8192_bf16.md")
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_NAMES = {1: "gemm_persistent_ws", 2: "gemm_pair_ws"}   # by tg variant
 
 
 def parse_args(argv=None):
@@ -199,13 +200,15 @@ def parse_clock_csv(lines, t0, t1):
             "samples": len(inside)}
 
 
-def profile_traffic():
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, or None if
-    the kernel sources changed since that capture."""
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` from its committed ncu summary
+    (profiles/<kernel>_<size>_<dtype>.md), or None if there is none or the library's sources
+    changed since that capture."""
     from persistent_warp_specialized_gb300 import _build
 
+    tag = workload.replace("gemm_", "")
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(PROFILES, f"{kernel}_{tag}.md")).read()
     except OSError:
         return None
     vals = {}
@@ -366,6 +369,8 @@ def run_tg(args):
     e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    launch = tg.tg_gemm_launch_shape(w.M, w.N, w.K, args.variant)
+    kernel = KERNEL_NAMES[launch["variant"]]
     peaks, peak_src = measured_peaks()
     achieved = w.flops / (ms_local * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -374,7 +379,8 @@ def run_tg(args):
     else:
         peak_note = "bf16 burst peak"
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": profile_traffic(),
+                "frac": achieved / peak, "kernel": kernel,
+                "traffic": profile_traffic(kernel, w.name),
                 "peak_source": f"{peak_src} ({peak_note}, cuBLAS torch.matmul)",
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                 "frac_of_nominal_dense": achieved / NOMINAL_DENSE_BF16_TFLOPS,
@@ -389,7 +395,7 @@ def run_tg(args):
         "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see config.inputs)",
         "config": dict(workload_config(w), sms=sms,
-                       launch=tg.tg_gemm_launch_shape(w.M, w.N, w.K, args.variant)),
+                       launch=launch),
         "gpu_launches": steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
     }
 
