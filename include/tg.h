@@ -38,12 +38,17 @@ extern "C" {
 /* element types: input, output and (internally) fp32 accumulation */
 enum { TG_F16 = 0, TG_BF16 = 1 };
 
-/* kernel variants (tg_gemm_persistent_ex, tg_gemm_persistent_debug) */
+/* kernel variants (tg_gemm_persistent_ex, tg_gemm_persistent_debug, tg_gemm_launch_shape) */
 enum {
   TG_VARIANT_AUTO = 0,    /* the library's choice for the problem (what tg_gemm_persistent runs) */
   TG_VARIANT_SINGLE = 1,  /* one CTA per 128 x 256 output tile, tcgen05 cta_group::1 */
-  TG_VARIANT_PAIR = 2     /* a CTA pair per 256 x 256 output tile, tcgen05 cta_group::2
+  TG_VARIANT_PAIR = 2,    /* a CTA pair per 256 x 256 output tile, tcgen05 cta_group::2
                              ("[Feature] Introduce tile scheduler #2441", gemm_persistent_2cta) */
+  /* OR'ed into a variant: walk tiles exactly as the page's scheduler does.  By default, when
+     the last partial wave of tiles would keep at most half of the workers busy, each of its
+     tiles is cut into two half-width (N) units so that wave takes half a tile's time; see
+     tg_tile_schedule_ex. */
+  TG_SCHEDULE_PLAIN = 0x100
 };
 
 /* status codes */
@@ -91,6 +96,20 @@ int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
  */
 int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host);
 
+/*
+ * tg_tile_schedule_ex -- the unit order of the GEMM kernel, with or without the tail split.
+ *   split_tail = 0: the rows of tg_tile_schedule, each with part = -1.
+ *   split_tail != 0: with T = m_blocks * n_blocks tiles and R = T mod num_sms, if
+ *     0 < 2R <= num_sms the last R tiles of the grouped order become 2R half-width units:
+ *     unit ids 0 .. T-R-1 are whole tiles (part -1), unit T-R+2i+h is half h (0 = left,
+ *     1 = right, in N) of tile T-R+i; workers step through unit ids with the grid stride.
+ *   out_host: HOST buffer of 5 int32 per unit (there are at most 2 * m_blocks * n_blocks units),
+ *     rows (worker, w, bx, by, part) ordered by worker, then w.
+ * Synchronous.  Returns the number of units (rows) or an error.
+ */
+int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int split_tail,
+                        int32_t* out_host);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* tg_last_error(void);
 
@@ -102,23 +121,25 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
 
 /*
  * tg_gemm_launch_shape -- the persistent launch the library would use for an M x N x K
- * problem on the current device with ``variant`` (TG_VARIANT_*; AUTO is resolved).
+ * problem on the current device with ``variant`` (TG_VARIANT_*, optionally | TG_SCHEDULE_PLAIN;
+ * AUTO is resolved).
  *   *variant_out: the concrete variant; *tile_m, *tile_n: the output tile of one scheduler
  *   worker; *m_tiles, *n_tiles: the tile grid; *workers: scheduler workers (CTAs for SINGLE,
- *   CTA pairs for PAIR); *ctas: CTAs launched.  Any pointer may be NULL.
+ *   CTA pairs for PAIR); *ctas: CTAs launched; *split_from, *units: the tail split (units
+ *   below split_from are whole tiles; split_from == units: no split).  Any pointer may be NULL.
  * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
  */
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
-                         int* ctas);
+                         int* ctas, int* split_from, int* units);
 
 /*
  * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
  *   variant: TG_VARIANT_* as in tg_gemm_persistent_ex.
- *   trace_dev: NULL or a device buffer of 4 int32 per output tile of the variant (128 x 256
- *     tiles for SINGLE, 256 x 256 for PAIR); row t (t = the linear tile id) receives
- *     (worker, w, bx, by) as the epilogue that stored tile t saw them (worker = CTA, or CTA
- *     pair) -- evidence that the kernel followed the schedule of tg_tile_schedule.
+ *   trace_dev: NULL or a device buffer of 5 int32 per work unit (tg_gemm_launch_shape's
+ *     *units); row u (the unit id) receives (worker, w, bx, by, part) as the epilogue that
+ *     stored unit u saw them (worker = CTA, or CTA pair) -- evidence that the kernel followed
+ *     the schedule of tg_tile_schedule_ex.
  *   watchdog_ns: limit for every wait inside the kernel (0 = the default of about 4 s).
  *   inject_skip_phase: -1 for none; otherwise CTA 0's producer never arms or fills that
  *     pipeline phase, so the MMA role's wait on it cannot complete: the watchdog must fire, every

@@ -56,3 +56,50 @@ def enumerate_schedule(m_blocks, n_blocks, num_workers, group):
             rows.append((c, w, bx, by))
             w += 1
     return rows
+
+
+def tail_split_point(m_blocks, n_blocks, num_workers):
+    """(F, units): tiles 0..F-1 stay whole; when the last partial wave holds R = T - F tiles
+    with 0 < 2R <= P, each of those R tiles becomes two half-width units, else F = T."""
+    total = m_blocks * n_blocks
+    rem = total % num_workers
+    if rem == 0 or 2 * rem > num_workers:
+        return total, total
+    first = total - rem
+    return first, first + 2 * rem
+
+
+def unit_tile(u, m_blocks, n_blocks, group, first_split):
+    """Unit id -> (bx, by, part): part -1 is a whole tile, 0 / 1 the left / right half (in N)
+    of tile first_split + (u - first_split) // 2."""
+    if u < first_split:
+        bx, by = tile_coord(u, m_blocks, n_blocks, group)
+        return bx, by, -1
+    t = first_split + (u - first_split) // 2
+    bx, by = tile_coord(t, m_blocks, n_blocks, group)
+    return bx, by, (u - first_split) % 2
+
+
+def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True):
+    """Rows (worker, w, bx, by, part) of the persistent traversal over work units, ordered
+    by worker, then w.  Without the split (or when it does not apply) every unit is a whole
+    tile and the rows are those of enumerate_schedule with part = -1.
+
+    Reading beyond the pages (the grouped traversal itself is the page's): the last partial
+    wave, if at most half the workers would be busy in it, is cut into half-width units so
+    that it takes half a tile's time; unit ids keep the grid stride c, c + P, ...
+    """
+    if min(m_blocks, n_blocks, num_workers, group) < 1:
+        raise ValueError("m_blocks, n_blocks, num_workers and group must be >= 1")
+    if split_tail:
+        first, units = tail_split_point(m_blocks, n_blocks, num_workers)
+    else:
+        first = units = m_blocks * n_blocks
+    rows = []
+    for c in range(num_workers):
+        w = 0
+        while c + w * num_workers < units:
+            bx, by, part = unit_tile(c + w * num_workers, m_blocks, n_blocks, group, first)
+            rows.append((c, w, bx, by, part))
+            w += 1
+    return rows

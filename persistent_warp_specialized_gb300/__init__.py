@@ -25,6 +25,7 @@ TG_ERR_TIMEOUT = -4
 TG_VARIANT_AUTO = 0
 TG_VARIANT_SINGLE = 1
 TG_VARIANT_PAIR = 2
+TG_SCHEDULE_PLAIN = 0x100
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
@@ -33,6 +34,7 @@ EXPORTED = (
     "tg_gemm_persistent",
     "tg_gemm_persistent_ex",
     "tg_tile_schedule",
+    "tg_tile_schedule_ex",
     "tg_last_error",
     "tg_gemm_config",
     "tg_gemm_launch_shape",
@@ -67,12 +69,14 @@ def load_library(path=LIB_PATH):
     lib.tg_gemm_persistent_ex.restype = i32
     lib.tg_tile_schedule.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.tg_tile_schedule.restype = i32
+    lib.tg_tile_schedule_ex.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.tg_tile_schedule_ex.restype = i32
     lib.tg_last_error.argtypes = []
     lib.tg_last_error.restype = ctypes.c_char_p
     ip = ctypes.POINTER(ctypes.c_int)
     lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
     lib.tg_gemm_config.restype = i32
-    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32, ip, ip, ip, ip, ip, ip, ip]
+    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32, ip, ip, ip, ip, ip, ip, ip, ip, ip]
     lib.tg_gemm_launch_shape.restype = i32
     lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
                                              i64]
@@ -127,21 +131,25 @@ def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
 
 
-def _variant(v):
-    return VARIANTS[v] if isinstance(v, str) else int(v)
+def _variant(v, plain=False):
+    """"auto" / "single" / "pair" (or a TG_VARIANT_* int); ``plain`` adds TG_SCHEDULE_PLAIN."""
+    code = VARIANTS[v] if isinstance(v, str) else int(v)
+    return code | (TG_SCHEDULE_PLAIN if plain else 0)
 
 
-def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto"):
-    """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair")."""
+def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False):
+    """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
+    ``plain`` walks the page's tile order with no tail split."""
     return _check(load_library().tg_gemm_persistent_ex(
-        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _variant(variant)))
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
+        _variant(variant, plain)))
 
 
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
-                             watchdog_ns=0, inject_skip_phase=-1):
+                             watchdog_ns=0, inject_skip_phase=-1, plain=False):
     return _check(load_library().tg_gemm_persistent_debug(
-        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream), _variant(variant),
-        _ptr(trace), watchdog_ns, inject_skip_phase))
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
+        _variant(variant, plain), _ptr(trace), watchdog_ns, inject_skip_phase))
 
 
 def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,
@@ -162,12 +170,13 @@ def tg_gemm_config():
     return dict(zip(keys, (v.value for v in vals)))
 
 
-def tg_gemm_launch_shape(M, N, K, variant="auto"):
+def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False):
     """The persistent launch the library uses for M x N x K on the current device."""
-    vals = [ctypes.c_int() for _ in range(7)]
-    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant),
+    vals = [ctypes.c_int() for _ in range(9)]
+    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant, plain),
                                                *[ctypes.byref(v) for v in vals]))
-    keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas")
+    keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas",
+            "split_from", "units")
     return dict(zip(keys, (v.value for v in vals)))
 
 
@@ -177,6 +186,15 @@ def tg_tile_schedule(m_blocks, n_blocks, num_sms, group):
     buf = (ctypes.c_int32 * (4 * max(rows, 1)))()
     n = _check(load_library().tg_tile_schedule(m_blocks, n_blocks, num_sms, group, buf))
     return [tuple(buf[4 * i: 4 * i + 4]) for i in range(n)]
+
+
+def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True):
+    """Rows (worker, w, bx, by, part) of the device scheduler over work units."""
+    rows = 2 * max(0, m_blocks) * max(0, n_blocks)
+    buf = (ctypes.c_int32 * (5 * max(rows, 1)))()
+    n = _check(load_library().tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group,
+                                                  1 if split_tail else 0, buf))
+    return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
 
 
 def gemm(a, b, out=None, stream=None):

@@ -17,6 +17,7 @@
 #include "../../include/tg.h"
 #include "tg_config.h"
 #include "tg_internal.h"
+#include "tg_tile_scheduler.cuh"
 
 namespace {
 
@@ -176,29 +177,42 @@ int auto_variant(int64_t /*M*/, int64_t /*N*/, int64_t /*K*/, int max_pairs) {
 }
 
 struct Shape {
-  uint32_t tile_m, tile_n, m_tiles, n_tiles, workers, ctas;
+  uint32_t tile_m, tile_n, m_tiles, n_tiles, workers, ctas, split_from, units;
 };
 
 // Persistent launch of a concrete variant: one worker per SM (SINGLE) or per resident CTA
-// pair (PAIR), never more workers than tiles.
-Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, int sms, int max_pairs) {
+// pair (PAIR), never more workers than work units; the last partial wave is split into
+// half-width units unless ``plain`` (the page's traversal) is asked for.
+Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain, int sms,
+                   int max_pairs) {
   Shape sh;
   sh.tile_m = variant == TG_VARIANT_PAIR ? tg::kPairBM : tg::kBM;
   sh.tile_n = tg::kBN;
   sh.m_tiles = static_cast<uint32_t>((M + sh.tile_m - 1) / sh.tile_m);
   sh.n_tiles = static_cast<uint32_t>((N + sh.tile_n - 1) / sh.tile_n);
-  const uint64_t tiles = uint64_t(sh.m_tiles) * sh.n_tiles;
-  const uint64_t slots = variant == TG_VARIANT_PAIR ? uint64_t(max_pairs) : uint64_t(sms);
-  sh.workers = static_cast<uint32_t>(tiles < slots ? tiles : slots);
+  const uint32_t tiles = sh.m_tiles * sh.n_tiles;
+  const uint32_t slots = variant == TG_VARIANT_PAIR ? uint32_t(max_pairs) : uint32_t(sms);
+  if (plain) {
+    sh.split_from = sh.units = tiles;
+  } else {
+    tg::PersistentTileScheduler::tail_split(tiles, slots, sh.split_from, sh.units);
+  }
+  sh.workers = sh.units < slots ? sh.units : slots;
   sh.ctas = variant == TG_VARIANT_PAIR ? 2 * sh.workers : sh.workers;
   return sh;
+}
+
+bool known_variant(int v) {
+  const int kernel = v & ~TG_SCHEDULE_PLAIN;
+  return kernel == TG_VARIANT_AUTO || kernel == TG_VARIANT_SINGLE || kernel == TG_VARIANT_PAIR;
 }
 
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
               void* stream, int variant, bool debug, int32_t* trace, uint64_t watchdog_ns,
               int64_t inject) {
-  if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
-    return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
+  variant &= ~TG_SCHEDULE_PLAIN;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
   if (rc != TG_OK || nothing) return rc;
@@ -220,9 +234,11 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
-  const Shape sh = launch_shape(M, N, K, variant, sms, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, plain, sms, max_pairs);
   l.m_blocks = sh.m_tiles;
   l.n_blocks = sh.n_tiles;
+  l.split_from = sh.split_from;
+  l.total_units = sh.units;
   l.k_blocks = static_cast<uint32_t>((K + tg::kBK - 1) / tg::kBK);
   l.group = tg::kGroup;
   l.grid = sh.ctas;
@@ -262,16 +278,17 @@ int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev, int
 
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
-                         int* ctas) {
-  if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
-    return fail(TG_ERR_ARG, "unknown variant %d", variant);
+                         int* ctas, int* split_from, int* units) {
+  if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
+  variant &= ~TG_SCHEDULE_PLAIN;
   if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
   int sms = 0, max_pairs = 0;
   int rc = device_ready(&sms, &max_pairs);
   if (rc != TG_OK) return rc;
   if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
-  const Shape sh = launch_shape(M, N, K, variant, sms, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, plain, sms, max_pairs);
   if (variant_out) *variant_out = variant;
   if (tile_m) *tile_m = static_cast<int>(sh.tile_m);
   if (tile_n) *tile_n = static_cast<int>(sh.tile_n);
@@ -279,6 +296,8 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
   if (n_tiles) *n_tiles = static_cast<int>(sh.n_tiles);
   if (workers) *workers = static_cast<int>(sh.workers);
   if (ctas) *ctas = static_cast<int>(sh.ctas);
+  if (split_from) *split_from = static_cast<int>(sh.split_from);
+  if (units) *units = static_cast<int>(sh.units);
   return TG_OK;
 }
 
@@ -293,22 +312,52 @@ int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, 
                    watchdog_ns, inject_skip_phase);
 }
 
-int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host) {
-  if (m_blocks < 1 || n_blocks < 1 || num_sms < 1 || group < 1)
-    return fail(TG_ERR_ARG, "m_blocks, n_blocks, num_sms and group must be >= 1");
-  if (int64_t(m_blocks) * n_blocks > kMaxDim) return fail(TG_ERR_ARG, "too many tiles");
-  if (!out_host) return fail(TG_ERR_ARG, "null output buffer");
-  const uint64_t rows = uint64_t(m_blocks) * n_blocks;
-  const size_t bytes = rows * 4 * sizeof(int32_t);
+// Runs the device scheduler over [0, units) and copies rows of ``width`` int32 (4: without
+// the part column, 5: with it) to the host.
+int schedule_rows(int m_blocks, int n_blocks, int num_sms, int group, uint32_t split_from,
+                  uint32_t units, int width, int32_t* out_host) {
+  const uint64_t rows = units;
   int32_t* d = nullptr;
-  cudaError_t e = cudaMalloc(&d, bytes);
+  cudaError_t e = cudaMalloc(&d, rows * 5 * sizeof(int32_t));
   if (e != cudaSuccess) return fail_cuda("cudaMalloc", e);
-  e = tg::launch_tile_schedule(m_blocks, n_blocks, num_sms, group, d, nullptr);
-  if (e == cudaSuccess) e = cudaMemcpy(out_host, d, bytes, cudaMemcpyDeviceToHost);
+  e = tg::launch_tile_schedule(m_blocks, n_blocks, num_sms, group, split_from, units, d, nullptr);
+  if (e == cudaSuccess) {
+    if (width == 5) {
+      e = cudaMemcpy(out_host, d, rows * 5 * sizeof(int32_t), cudaMemcpyDeviceToHost);
+    } else {  // drop the part column: a strided 2-D copy of 4 of every 5 int32
+      e = cudaMemcpy2D(out_host, 4 * sizeof(int32_t), d, 5 * sizeof(int32_t), 4 * sizeof(int32_t),
+                       rows, cudaMemcpyDeviceToHost);
+    }
+  }
   cudaError_t e2 = cudaFree(d);
   if (e != cudaSuccess) return fail_cuda("tile schedule", e);
   if (e2 != cudaSuccess) return fail_cuda("cudaFree", e2);
   return static_cast<int>(rows);
+}
+
+int check_schedule_args(int m_blocks, int n_blocks, int num_sms, int group, const void* out) {
+  if (m_blocks < 1 || n_blocks < 1 || num_sms < 1 || group < 1)
+    return fail(TG_ERR_ARG, "m_blocks, n_blocks, num_sms and group must be >= 1");
+  if (int64_t(m_blocks) * n_blocks > (int64_t(1) << 30)) return fail(TG_ERR_ARG, "too many tiles");
+  if (!out) return fail(TG_ERR_ARG, "null output buffer");
+  return TG_OK;
+}
+
+int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t* out_host) {
+  int rc = check_schedule_args(m_blocks, n_blocks, num_sms, group, out_host);
+  if (rc != TG_OK) return rc;
+  const uint32_t tiles = uint32_t(m_blocks) * uint32_t(n_blocks);
+  return schedule_rows(m_blocks, n_blocks, num_sms, group, tiles, tiles, 4, out_host);
+}
+
+int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int split_tail,
+                        int32_t* out_host) {
+  int rc = check_schedule_args(m_blocks, n_blocks, num_sms, group, out_host);
+  if (rc != TG_OK) return rc;
+  const uint32_t tiles = uint32_t(m_blocks) * uint32_t(n_blocks);
+  uint32_t first = tiles, units = tiles;
+  if (split_tail) tg::PersistentTileScheduler::tail_split(tiles, uint32_t(num_sms), first, units);
+  return schedule_rows(m_blocks, n_blocks, num_sms, group, first, units, 5, out_host);
 }
 
 const char* tg_last_error(void) { return g_err; }

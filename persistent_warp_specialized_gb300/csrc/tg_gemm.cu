@@ -13,21 +13,22 @@ namespace {
 // (worker, w, bx, by); rows are ordered by worker, then w.  Worker c owns
 // q + (c < r) tiles where total = q * P + r, so its first row is c * q + min(c, r).
 __global__ void tile_schedule_kernel(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
-                                     uint32_t group, int32_t* __restrict__ out) {
+                                     uint32_t group, uint32_t split_from, uint32_t units,
+                                     int32_t* __restrict__ out) {
   const uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= num_workers) return;
-  const uint32_t total = m_blocks * n_blocks;
-  const uint32_t q = total / num_workers;
-  const uint32_t r = total % num_workers;
+  const uint32_t q = units / num_workers;
+  const uint32_t r = units % num_workers;
   uint64_t row = static_cast<uint64_t>(c) * q + (c < r ? c : r);
-  PersistentTileScheduler sched(m_blocks, n_blocks, group, num_workers);
+  PersistentTileScheduler sched(m_blocks, n_blocks, group, num_workers, split_from, units);
   sched.init(c);
   while (sched.valid()) {
-    int32_t* o = out + 4 * row;
+    int32_t* o = out + 5 * row;
     o[0] = static_cast<int32_t>(c);
     o[1] = static_cast<int32_t>(sched.current_iter);
     o[2] = static_cast<int32_t>(sched.m_idx);
     o[3] = static_cast<int32_t>(sched.n_idx);
+    o[4] = sched.part;
     ++row;
     sched.next_tile();
   }
@@ -50,6 +51,8 @@ GemmParams params_of(const GemmLaunch& l) {
   p.n_blocks = l.n_blocks;
   p.k_blocks = l.k_blocks;
   p.group = l.group;
+  p.split_from = l.split_from;
+  p.total_units = l.total_units;
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
   p.inject_skip_phase = l.inject_skip_phase;
@@ -128,11 +131,12 @@ cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {
 }
 
 cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
-                                 uint32_t group, int32_t* out_dev, cudaStream_t stream) {
+                                 uint32_t group, uint32_t split_from, uint32_t units,
+                                 int32_t* out_dev, cudaStream_t stream) {
   const uint32_t threads = 128;
   const uint32_t blocks = (num_workers + threads - 1) / threads;
   tile_schedule_kernel<<<blocks, threads, 0, stream>>>(m_blocks, n_blocks, num_workers, group,
-                                                       out_dev);
+                                                       split_from, units, out_dev);
   return cudaGetLastError();
 }
 

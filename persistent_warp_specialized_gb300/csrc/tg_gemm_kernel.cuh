@@ -51,8 +51,9 @@ struct GemmParams {
   void* C;                     // output base (used by the direct-store epilogue)
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
+  uint32_t split_from, total_units;   // tail split of the scheduler (see tg_tile_scheduler.cuh)
   uint64_t watchdog_ns;
-  int32_t* trace;              // debug instantiation only; may be null
+  int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
 };
 
@@ -236,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
+                                    p.total_units);
       sched.init(blockIdx.x);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
@@ -245,8 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
+        const bool half = sched.part >= 0;              // half-width unit of the tail split
         const int32_t m0 = static_cast<int32_t>(sched.m_idx) * kBM;
-        const int32_t n0 = static_cast<int32_t>(sched.n_idx) * kBN;
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
+        const uint32_t b_chunks = half ? kBN / kBChunkCols / 2 : kBN / kBChunkCols;
+        const uint32_t tx_bytes = kABytes + b_chunks * kBChunkBytes;
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = w * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kStages);
@@ -259,12 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
             continue;  // injected fault: this phase is never filled
           const uint32_t full = bar_loaded + 8u * s;
-          mbar_arrive_expect_tx(full, kStageBytes);
+          mbar_arrive_expect_tx(full, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
           load_operand(sA0 + s * kStageBytes, &tmA, full, kx, m0, pol_a, kAPolicy);
 #pragma unroll
           for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
-            load_operand(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
+            if (c < b_chunks)
+              load_operand(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
                          n0 + static_cast<int32_t>(c * kBChunkCols), kx, pol_b, kBPolicy);
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);
@@ -281,8 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(DT, kBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
-      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+      constexpr uint32_t idesc_full = idesc_f16(DT, kBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
+      constexpr uint32_t idesc_half = idesc_f16(DT, kBM, kBN / 2, 0, 1);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
+                                    p.total_units);
       sched.init(blockIdx.x);
       bool ok = true;
       while (ok && sched.valid()) {
@@ -295,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBN;
+        const uint32_t idesc = sched.part >= 0 ? idesc_half : idesc_full;
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kStages);
@@ -330,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp - kFirstEpiWarp;       // TMEM lanes 32q .. 32q + 31
-    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x);
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
+                                    p.total_units);
     sched.init(blockIdx.x);
     uint32_t chunk = 0;
     while (sched.valid()) {
@@ -340,14 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
+      const bool half = sched.part >= 0;
       const int32_t row0 = static_cast<int32_t>(sched.m_idx) * kBM + static_cast<int32_t>(q) * 32;
-      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN;
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
+      const uint32_t chunks = half ? kBN / kEpiN / 2 : kBN / kEpiN;
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kBN;
 #pragma unroll 1
-      for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+      for (uint32_t j = 0; j < chunks; ++j, ++chunk) {
         uint32_t v[64];
         tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
-        if (j == kBN / kEpiN - 1) {
+        if (j == chunks - 1) {
           // accumulator fully in registers: hand it back to the MMA warp before storing
           tcgen05_fence_before_sync();
           mbar_arrive(bar_tmem_empty + 8u * buf);
@@ -357,11 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  col0 + static_cast<int32_t>(j * kEpiN));
       }
       if (DEBUG && p.trace != nullptr && q == 0 && lane == 0) {
-        int32_t* tr = p.trace + 4ull * sched.linear_idx;
+        int32_t* tr = p.trace + 5ull * sched.linear_idx;
         tr[0] = static_cast<int32_t>(blockIdx.x);
         tr[1] = static_cast<int32_t>(w);
         tr[2] = static_cast<int32_t>(sched.m_idx);
         tr[3] = static_cast<int32_t>(sched.n_idx);
+        tr[4] = sched.part;
       }
       sched.next_tile();
     }

@@ -136,7 +136,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units);
       sched.init(pair);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
@@ -144,8 +145,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
+        const bool half = sched.part >= 0;          // half-width unit of the tail split
         const int32_t m0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM);
-        const int32_t n0 = static_cast<int32_t>(sched.n_idx * kBN + rank * kPairBNHalf);
+        // whole unit: CTA r loads columns [128 r, 128 r + 128) of the 256-wide tile;
+        // half unit (128 wide, starting at 128 * part): CTA r loads [64 r, 64 r + 64) of it
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx * kBN) +
+                           (half ? sched.part * (kBN / 2) + static_cast<int32_t>(rank) * (kPairBNHalf / 2)
+                                 : static_cast<int32_t>(rank) * kPairBNHalf);
+        const uint32_t b_chunks = half ? kPairBNHalf / kBChunkCols / 2 : kPairBNHalf / kBChunkCols;
+        const uint32_t tx_bytes = 2u * (kABytes + b_chunks * kBChunkBytes);
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = w * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
@@ -159,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
             continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
-          if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, kPairTxBytes);
+          if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
           if (kAPolicy != 0)
             tma_load_2d_pair_hint(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0, pol_a);
@@ -167,6 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0);
 #pragma unroll
           for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c) {
+            if (c >= b_chunks) break;
             const uint32_t dst = sB0 + s * kPairStageBytes + c * kBChunkBytes;
             const int32_t nx = n0 + static_cast<int32_t>(c * kBChunkCols);
             if (kBPolicy != 0)
@@ -195,8 +204,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
-      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+      constexpr uint32_t idesc_full = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
+      constexpr uint32_t idesc_half = idesc_f16(DT, kPairBM, kBN / 2, 0, 1);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units);
       sched.init(pair);
       bool ok = true;
       while (ok && sched.valid()) {
@@ -209,6 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBN;
+        const uint32_t idesc = sched.part >= 0 ? idesc_half : idesc_full;
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
@@ -240,7 +252,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t q = warp - kFirstEpiWarp;
-    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs);
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units);
     sched.init(pair);
     uint32_t chunk = 0;
     while (sched.valid()) {
@@ -250,15 +263,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           peer_abort, limit, kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
+      const bool half = sched.part >= 0;
       const int32_t row0 =
           static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM + q * 32u);
-      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN;
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
+      const uint32_t chunks = half ? kBN / kEpiN / 2 : kBN / kEpiN;
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kBN;
 #pragma unroll 1
-      for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+      for (uint32_t j = 0; j < chunks; ++j, ++chunk) {
         uint32_t v[64];
         tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
-        if (j == kBN / kEpiN - 1) {
+        if (j == chunks - 1) {
           tcgen05_fence_before_sync();
           mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * buf, 0));
         }
@@ -267,11 +282,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  col0 + static_cast<int32_t>(j * kEpiN));
       }
       if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
-        int32_t* tr = p.trace + 4ull * sched.linear_idx;
+        int32_t* tr = p.trace + 5ull * sched.linear_idx;
         tr[0] = static_cast<int32_t>(pair);
         tr[1] = static_cast<int32_t>(w);
         tr[2] = static_cast<int32_t>(sched.m_idx);
         tr[3] = static_cast<int32_t>(sched.n_idx);
+        tr[4] = sched.part;
       }
       sched.next_tile();
     }

@@ -18,6 +18,13 @@
 // [0, m_blocks * n_blocks).  With p = t / (m_blocks * g), width = min(g, n_blocks - p * g)
 // and u = t - p * m_blocks * g, a tile is (u / width, p * g + u % width); on full panels
 // this equals the page's formula term for term.
+//
+// Tail split (an addition to the page's scheduler): the workers step through *units*, not
+// tiles.  Units 0 .. split_from - 1 are the tiles with the same ids; when the last partial
+// wave would keep at most half of the workers busy, its tiles (ids split_from .. T - 1) are
+// each cut into two half-width units (part 0 = left, part 1 = right half in N), numbered
+// split_from + 2 (t - split_from) + part, so that wave takes half a tile's time.  Without a
+// split, split_from = total_units = T and every unit is the page's tile (part = -1).
 #pragma once
 
 #include <cstdint>
@@ -25,14 +32,35 @@
 namespace tg {
 
 struct PersistentTileScheduler {
-  uint32_t m_blocks, n_blocks, group, num_workers, total;
-  uint32_t current_iter;  // w: tiles this worker has already taken
+  uint32_t m_blocks, n_blocks, group, num_workers;
+  uint32_t split_from;    // first unit id that is half a tile
+  uint32_t total_units;   // units in the traversal
+  uint32_t current_iter;  // w: units this worker has already taken
   uint32_t linear_idx;    // worker + w * num_workers
   uint32_t m_idx, n_idx;  // decoded tile (valid only while valid())
+  int32_t part;           // -1 whole tile, 0 / 1 left / right half in N
 
+  // the page's traversal: every unit a whole tile
   __host__ __device__ PersistentTileScheduler(uint32_t m, uint32_t n, uint32_t g, uint32_t p)
-      : m_blocks(m), n_blocks(n), group(g), num_workers(p), total(m * n),
-        current_iter(0), linear_idx(0), m_idx(0), n_idx(0) {}
+      : PersistentTileScheduler(m, n, g, p, m * n, m * n) {}
+
+  __host__ __device__ PersistentTileScheduler(uint32_t m, uint32_t n, uint32_t g, uint32_t p,
+                                              uint32_t first_split, uint32_t units)
+      : m_blocks(m), n_blocks(n), group(g), num_workers(p), split_from(first_split),
+        total_units(units), current_iter(0), linear_idx(0), m_idx(0), n_idx(0), part(-1) {}
+
+  // (split_from, total_units) for T tiles over P workers: split the last partial wave when
+  // it holds R tiles with 0 < 2R <= P.
+  __host__ __device__ static void tail_split(uint32_t tiles, uint32_t workers,
+                                             uint32_t& first_split, uint32_t& units) {
+    const uint32_t rem = tiles % workers;
+    if (rem == 0 || 2 * rem > workers) {
+      first_split = units = tiles;
+    } else {
+      first_split = tiles - rem;
+      units = first_split + 2 * rem;
+    }
+  }
 
   __host__ __device__ static void coord(uint32_t t, uint32_t m_blocks, uint32_t n_blocks,
                                         uint32_t group, uint32_t& bx, uint32_t& by) {
@@ -47,7 +75,15 @@ struct PersistentTileScheduler {
   }
 
   __host__ __device__ void decode() {
-    if (linear_idx < total) coord(linear_idx, m_blocks, n_blocks, group, m_idx, n_idx);
+    if (linear_idx >= total_units) return;
+    if (linear_idx < split_from) {
+      coord(linear_idx, m_blocks, n_blocks, group, m_idx, n_idx);
+      part = -1;
+    } else {
+      const uint32_t v = linear_idx - split_from;
+      coord(split_from + v / 2, m_blocks, n_blocks, group, m_idx, n_idx);
+      part = static_cast<int32_t>(v & 1u);
+    }
   }
 
   __host__ __device__ void init(uint32_t worker) {
@@ -56,7 +92,7 @@ struct PersistentTileScheduler {
     decode();
   }
 
-  __host__ __device__ bool valid() const { return linear_idx < total; }
+  __host__ __device__ bool valid() const { return linear_idx < total_units; }
 
   __host__ __device__ void next_tile() {
     ++current_iter;

@@ -93,6 +93,25 @@ def test_all_ones_give_k(dtype, K, variant):
     assert np.array_equal(formats.decode(c, dtype), np.full((M, N), float(K)))
 
 
+@pytest.mark.parametrize("plain", [False, True])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_split_tail_after_full_waves_is_bit_exact(variant, plain):
+    # 2560 x 2560: 200 single tiles (152 + a last wave of 48) or 100 pair tiles (76 + 24):
+    # the last wave runs as half-width units unless the plain page order is asked for
+    M, N, K = 2560, 2560, 448
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
+    assert (shape["units"] > shape["split_from"]) == (not plain)
+    a, b = wl.small_int_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=11)
+    M_, K_ = a.shape
+    a_d, b_d = a.cuda(), b.cuda()
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_persistent_ex(a_d, b_d, c, M, N, K, "bf16", variant=variant, plain=plain)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
+
+
 def test_k_zero_gives_zeros():
     c = torch.full((64, 64), 7.0, dtype=torch.bfloat16, device="cuda")
     a = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")

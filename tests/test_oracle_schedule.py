@@ -99,3 +99,53 @@ def test_bad_arguments():
         schedule.tile_coord(6, 2, 3, 8)
     with pytest.raises(ValueError):
         schedule.enumerate_schedule(0, 3, 4, 8)
+
+
+@pytest.mark.parametrize("workers", [1, 3, 7, 76, 148, 152])
+def test_units_cover_every_tile_exactly_once(workers):
+    # whole tiles plus half tiles: each tile is covered either once whole or by both halves
+    for m, n, g in itertools.product([1, 2, 5, 8, 13, 32], [1, 3, 4, 9, 28, 32], [1, 8]):
+        rows = schedule.enumerate_units(m, n, workers, g)
+        cover = {}
+        for (_, _, bx, by, part) in rows:
+            cover.setdefault((bx, by), []).append(part)
+        assert sorted(cover) == [(x, y) for x in range(m) for y in range(n)]
+        for parts in cover.values():
+            assert sorted(parts) in ([-1], [0, 1])
+
+
+def test_tail_split_only_when_the_last_wave_is_at_most_half_full():
+    # 8192^3 single tiles: 2048 = 13 * 152 + 72, 2 * 72 <= 152 -> split the last 72 tiles
+    assert schedule.tail_split_point(64, 32, 152) == (1976, 1976 + 144)
+    # 8192^3 pair tiles: 1024 = 13 * 76 + 36
+    assert schedule.tail_split_point(32, 32, 76) == (988, 988 + 72)
+    # 4000 x 7000 single: 896 = 5 * 152 + 136 and 2 * 136 > 152: no split
+    assert schedule.tail_split_point(32, 28, 152) == (896, 896)
+    # fewer tiles than workers: every tile is split when 2T <= P
+    assert schedule.tail_split_point(8, 4, 152) == (0, 64)
+    assert schedule.tail_split_point(8, 4, 76) == (0, 64)
+    assert schedule.tail_split_point(8, 8, 76) == (64, 64)
+    # exact waves: nothing to split
+    assert schedule.tail_split_point(8, 19, 152) == (152, 152)
+
+
+def test_units_without_split_are_the_page_schedule():
+    for m, n, p, g in [(64, 32, 152, 8), (32, 28, 148, 8), (8, 4, 148, 8), (5, 9, 7, 3)]:
+        plain = schedule.enumerate_units(m, n, p, g, split_tail=False)
+        assert plain == [r + (-1,) for r in schedule.enumerate_schedule(m, n, p, g)]
+
+
+def test_split_units_follow_the_grid_stride_and_the_grouped_order():
+    m, n, p, g = 64, 32, 152, 8
+    first, units = schedule.tail_split_point(m, n, p)
+    rows = schedule.enumerate_units(m, n, p, g)
+    for (c, w, bx, by, part) in rows:
+        u = c + w * p
+        if u < first:
+            assert part == -1 and (bx, by) == schedule.tile_coord(u, m, n, g)
+        else:
+            assert (bx, by) == schedule.tile_coord(first + (u - first) // 2, m, n, g)
+            assert part == (u - first) % 2
+    # workers' unit counts differ by at most one
+    counts = [sum(1 for r in rows if r[0] == c) for c in range(p)]
+    assert max(counts) - min(counts) <= 1

@@ -45,32 +45,44 @@ def test_schedule_matches_stored_fixture(name):
     assert got == rows
 
 
+def test_unit_schedule_brute_force_grids():
+    for m, n, g, p in itertools.product([1, 2, 5, 8, 13, 32, 64], [1, 3, 4, 9, 16, 28, 32],
+                                        [1, 8], [1, 7, 76, 148, 152]):
+        for split in (False, True):
+            got = tg.tg_tile_schedule_ex(m, n, p, g, split)
+            assert got == schedule.enumerate_units(m, n, p, g, split), (m, n, g, p, split)
+
+
 def test_config1_schedule_148_workers():
     # the 256^3 workload: 2 x 1 tiles over 148 workers, group 8
     assert tg.tg_tile_schedule(2, 1, wl.SCHEDULE_CHECK_WORKERS, wl.SCHEDULE_CHECK_GROUP) == [
         (0, 0, 0, 0), (1, 0, 1, 0)]
 
 
+@pytest.mark.parametrize("plain", [False, True])
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(4000, 7000, 256), (8192, 8192, 64), (1024, 1024, 1024),
-                                   (256, 256, 256), (4000, 2048, 128)])
-def test_kernel_followed_the_schedule(M, N, K, variant):
-    # the epilogue of the real GEMM records (worker, w, bx, by) for every tile it stored
-    shape = tg.tg_gemm_launch_shape(M, N, K, variant)
+                                   (256, 256, 256), (4000, 2048, 128), (2560, 2560, 128)])
+def test_kernel_followed_the_schedule(M, N, K, variant, plain):
+    # the epilogue of the real GEMM records (worker, w, bx, by, part) for every unit it stored
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
     m_tiles, n_tiles, workers = shape["m_tiles"], shape["n_tiles"], shape["workers"]
+    units = shape["units"]
     a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=M)
     a_d, b_d = a.cuda(), b.cuda()
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    trace = torch.full((m_tiles * n_tiles, 4), -1, dtype=torch.int32, device="cuda")
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
     assert tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
-                                       trace=trace) == 0
-    want = schedule.enumerate_schedule(m_tiles, n_tiles, workers, tg.tg_gemm_config()["group"])
-    by_tile = {}
-    for (worker, w, bx, by) in want:
-        by_tile[worker + w * workers] = (worker, w, bx, by)
+                                       trace=trace, plain=plain) == 0
+    want = schedule.enumerate_units(m_tiles, n_tiles, workers, tg.tg_gemm_config()["group"],
+                                    split_tail=not plain)
+    assert len(want) == units
+    by_unit = {}
+    for (worker, w, bx, by, part) in want:
+        by_unit[worker + w * workers] = (worker, w, bx, by, part)
     got = trace.cpu().numpy()
-    for t in range(m_tiles * n_tiles):
-        assert tuple(int(v) for v in got[t]) == by_tile[t], t
+    for u in range(units):
+        assert tuple(int(v) for v in got[u]) == by_unit[u], u
     # the debug build computes the same product
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "debug build")
 
