@@ -227,7 +227,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     return e == cudaSuccess ? TG_OK : fail_cuda("zero fill launch", e);
   }
   tg::GemmLaunch l;
-  if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kBK, tg::kBM, "A")) != TG_OK) return rc;
+  if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kKAtom, tg::kBM, "A")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, tg::kBK, "B")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
   l.C = C;

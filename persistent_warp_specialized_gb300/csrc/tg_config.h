@@ -25,7 +25,12 @@ constexpr int kBM = 128;
 #define TG_BN 256
 #endif
 constexpr int kBN = TG_BN;
-constexpr int kBK = 64;
+#ifndef TG_BK
+#define TG_BK 64
+#endif
+constexpr int kBK = TG_BK;               // a multiple of 64: kKAtoms 128-byte swizzle atoms
+constexpr int kKAtom = 64;               // K elements of one 128-byte swizzle row
+constexpr int kKAtoms = kBK / kKAtom;
 // Ring depths can be overridden at compile time (-DTG_STAGES=, -DTG_PAIR_STAGES=) to tune.
 #ifndef TG_STAGES
 #define TG_STAGES 4
@@ -59,7 +64,8 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kFirstEpiWarp = 4;
 
 constexpr uint32_t kElemBytes = 2;
-constexpr uint32_t kABytes = kBM * kBK * kElemBytes;             // 16 KiB
+constexpr uint32_t kAAtomBytes = kBM * kKAtom * kElemBytes;      // 16 KiB: one K atom of A
+constexpr uint32_t kABytes = kBM * kBK * kElemBytes;             // 16 KiB at block_K 64
 constexpr uint32_t kBBytes = kBK * kBN * kElemBytes;             // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;              // 48 KiB: expect_tx per stage
 constexpr uint32_t kBChunkCols = 64;                             // one 128-byte swizzle row of B
@@ -70,7 +76,8 @@ constexpr uint32_t kEpiSmemBytes = kEpiDirect ? 0u : kEpiWarps * 2 * kEpiBufByte
 constexpr uint32_t kSmemBytes = kSmemAlignSlack + kStages * kStageBytes + kEpiSmemBytes;
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(kBK * kElemBytes == 128, "block_K must span one 128-byte swizzle row");
+static_assert(kKAtom * kElemBytes == 128, "a K atom spans one 128-byte swizzle row");
+static_assert(kBK % kKAtom == 0 && kBK <= 256, "block_K: a multiple of 64, at most 256");
 static_assert(kEpiN * kElemBytes == 128, "store_block_N must span one 128-byte swizzle row");
 static_assert(kBN % kBChunkCols == 0 && kBN % kEpiN == 0, "block_N tiling");
 static_assert(kBM == 128 && kBN % 16 == 0 && kBN <= 256, "tcgen05.mma cta_group::1 shape");

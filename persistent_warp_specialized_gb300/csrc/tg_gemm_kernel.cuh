@@ -266,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = bar_loaded + 8u * s;
           mbar_arrive_expect_tx(full, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
-          load_operand(sA0 + s * kStageBytes, &tmA, full, kx, m0, pol_a, kAPolicy);
+#pragma unroll
+          for (uint32_t a = 0; a < kKAtoms; ++a)
+            load_operand(sA0 + s * kStageBytes + a * kAAtomBytes, &tmA, full,
+                         kx + static_cast<int32_t>(a * kKAtom), m0, pol_a, kAPolicy);
 #pragma unroll
           for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
             if (c < b_chunks)
@@ -317,11 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = sB0 + s * kStageBytes;
 #pragma unroll
           for (uint32_t kk = 0; kk < kBK / kUmmaK; ++kk) {
-            // A: K-major, advance 16 elements = 32 bytes inside the swizzle row;
-            //    SBO = 1024 bytes between 8-row groups.
-            // B: N-major, advance 16 K-rows = 2048 bytes; LBO = 8 KiB between 64-column
-            //    chunks, SBO = 1024 bytes between 8-row groups.
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+            // A: K-major, one 16 KiB atom per 64 K; inside an atom advance 16 elements =
+            //    32 bytes along the swizzle row; SBO = 1024 bytes between 8-row groups.
+            // B: N-major, advance 16 K-rows = 2048 bytes; LBO = one 64-column chunk
+            //    (block_K rows x 128 bytes) between chunks, SBO = 1024 bytes between 8-row groups.
+            const uint32_t a_off = (kk / (kKAtom / kUmmaK)) * kAAtomBytes +
+                                   (kk % (kKAtom / kUmmaK)) * kUmmaK * kElemBytes;
+            const uint64_t a_desc = smem_desc_sw128(a_addr + a_off, 16, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kBChunkBytes, 1024);
             umma_f16(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
           }

@@ -169,10 +169,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;
-          if (kAPolicy != 0)
-            tma_load_2d_pair_hint(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0, pol_a);
-          else
-            tma_load_2d_pair(sA0 + s * kPairStageBytes, &tmA, full_even, kx, m0);
+#pragma unroll
+          for (uint32_t a = 0; a < kKAtoms; ++a) {
+            const uint32_t dst = sA0 + s * kPairStageBytes + a * kAAtomBytes;
+            const int32_t ax = kx + static_cast<int32_t>(a * kKAtom);
+            if (kAPolicy != 0)
+              tma_load_2d_pair_hint(dst, &tmA, full_even, ax, m0, pol_a);
+            else
+              tma_load_2d_pair(dst, &tmA, full_even, ax, m0);
+          }
 #pragma unroll
           for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c) {
             if (c >= b_chunks) break;
@@ -235,7 +240,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = sB0 + s * kPairStageBytes;
 #pragma unroll
           for (uint32_t kk = 0; kk < kBK / kUmmaK; ++kk) {
-            const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+            const uint32_t a_off = (kk / (kKAtom / kUmmaK)) * kAAtomBytes +
+                                   (kk % (kKAtom / kUmmaK)) * kUmmaK * kElemBytes;
+            const uint64_t a_desc = smem_desc_sw128(a_addr + a_off, 16, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kBChunkBytes, 1024);
             umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
           }
