@@ -56,7 +56,10 @@ constexpr int kAPolicy = TG_A_POLICY;
 constexpr int kBPolicy = TG_B_POLICY;
 constexpr bool kEpiDirect = TG_EPI_DIRECT != 0;
 constexpr int kEpiN = 64;
-constexpr int kGroup = 8;
+#ifndef TG_GROUP
+#define TG_GROUP 8
+#endif
+constexpr int kGroup = TG_GROUP;         // the page's group_size
 constexpr int kThreads = 256;
 constexpr int kUmmaK = 16;                 // K of one tcgen05.mma kind::f16
 constexpr int kEpiWarps = 4;
