@@ -170,10 +170,12 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
   return TG_OK;
 }
 
-// The variant TG_VARIANT_AUTO resolves to.
-int auto_variant(int64_t /*M*/, int64_t /*N*/, int64_t /*K*/, int max_pairs) {
-  (void)max_pairs;
-  return TG_VARIANT_SINGLE;
+// The variant TG_VARIANT_AUTO resolves to: the CTA-pair kernel once its 256 x 256 tiles fill
+// at least one wave of resident pairs (measured faster there at every workload size), else
+// the single-CTA kernel, whose smaller tiles spread a small problem over more SMs.
+int auto_variant(int64_t M, int64_t N, int64_t /*K*/, int max_pairs) {
+  const int64_t pair_tiles = ((M + tg::kPairBM - 1) / tg::kPairBM) * ((N + tg::kBN - 1) / tg::kBN);
+  return (max_pairs > 0 && pair_tiles >= max_pairs) ? TG_VARIANT_PAIR : TG_VARIANT_SINGLE;
 }
 
 struct Shape {
@@ -228,7 +230,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   }
   tg::GemmLaunch l;
   if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kKAtom, tg::kBM, "A")) != TG_OK) return rc;
-  if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, tg::kBK, "B")) != TG_OK) return rc;
+  const int block_k = variant == TG_VARIANT_PAIR ? tg::kPairBK : tg::kBK;
+  if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, block_k, "B")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
   l.C = C;
   l.M = static_cast<uint32_t>(M);
@@ -239,7 +242,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.n_blocks = sh.n_tiles;
   l.split_from = sh.split_from;
   l.total_units = sh.units;
-  l.k_blocks = static_cast<uint32_t>((K + tg::kBK - 1) / tg::kBK);
+  l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
   l.group = tg::kGroup;
   l.grid = sh.ctas;
   l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;

@@ -36,7 +36,10 @@ constexpr int kKAtoms = kBK / kKAtom;
 #define TG_STAGES 4
 #endif
 #ifndef TG_PAIR_STAGES
-#define TG_PAIR_STAGES 6
+#define TG_PAIR_STAGES 3
+#endif
+#ifndef TG_PAIR_BK
+#define TG_PAIR_BK 128
 #endif
 // L2 policy of the A and B loads (0 none, 1 evict_first, 2 evict_last, 3 evict_normal)
 #ifndef TG_A_POLICY
@@ -90,17 +93,25 @@ static_assert(kSmemBytes + 256 <= 232448, "shared memory per CTA");
 // CTA-pair variant (tcgen05 cta_group::2, the page's gemm_persistent_2cta): a cluster of two
 // CTAs computes a 256 x 256 output tile.  CTA r of the pair loads A rows [128r, 128r + 128)
 // and B columns [128r, 128r + 128) of the tile; one 256 x 256 x 16 MMA issued by the even CTA
-// reads both halves, and each CTA's TMEM holds its 128 rows x 256 columns.  A stage is 32 KiB
-// per CTA, so six stages fit beside the same epilogue staging.
+// reads both halves, and each CTA's TMEM holds its 128 rows x 256 columns.  The pair takes
+// block_K = 128 per stage (64 KiB per CTA, three stages): measured on GB300, the fixed cost
+// of each stage hand-over (barrier waits, commit, refill) weighs less with eight MMAs per
+// stage than with four, more than the shallower ring costs (8192^3: +9 %, 4096^3: +15 %
+// over block_K 64 with six stages).
 constexpr int kPairBM = 2 * kBM;                                  // 256 rows per pair tile
 constexpr int kPairBNHalf = kBN / 2;                              // B columns one CTA loads
 constexpr int kPairStages = TG_PAIR_STAGES;
-constexpr uint32_t kPairBBytes = kBK * kPairBNHalf * kElemBytes;  // 16 KiB
-constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;       // 32 KiB per CTA
+constexpr int kPairBK = TG_PAIR_BK;
+constexpr int kPairKAtoms = kPairBK / kKAtom;
+constexpr uint32_t kPairABytes = kBM * kPairBK * kElemBytes;          // 32 KiB
+constexpr uint32_t kPairBChunkBytes = kPairBK * kBChunkCols * kElemBytes;  // 16 KiB
+constexpr uint32_t kPairBBytes = kPairBK * kPairBNHalf * kElemBytes;  // 32 KiB
+constexpr uint32_t kPairStageBytes = kPairABytes + kPairBBytes;       // 64 KiB per CTA
 constexpr uint32_t kPairTxBytes = 2 * kPairStageBytes;            // both CTAs' bytes, one barrier
 constexpr uint32_t kPairSmemBytes = kSmemAlignSlack + kPairStages * kPairStageBytes + kEpiSmemBytes;
 static_assert(kPairSmemBytes + 256 <= 232448, "shared memory per CTA (pair variant)");
 static_assert(kPairBNHalf % kBChunkCols == 0, "pair B half must be whole 64-column chunks");
+static_assert(kPairBK % kKAtom == 0 && kPairBK <= 256, "pair block_K: a multiple of 64, <= 256");
 
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;

@@ -13,9 +13,9 @@
 // there and its stores are clipped or skipped, so nothing outside A or C is touched (the
 // out-of-bounds ``bx`` the review of the PR warns about).
 //
-// Per CTA and k-block: A box 128 x 64 (16 KiB) and two B boxes 64 x 64 (16 KiB) into the
-// CTA's own ring slot; both CTAs' bytes complete on the even CTA's ``loaded[s]``, which the
-// even CTA arms with 64 KiB.  The MMA (M = 256, N = 256, K = 16, four per k-block) reads A
+// Per CTA and k-block of 128: two A boxes 128 x 64 (32 KiB) and two B boxes 64 x 128 (32 KiB)
+// into the CTA's own ring slot; both CTAs' bytes complete on the even CTA's ``loaded[s]``,
+// which the even CTA arms with 128 KiB.  The MMA (M = 256, N = 256, K = 16, eight per k-block) reads A
 // rows 0..127 and B columns 0..127 from the even CTA's slot and the rest from the odd
 // CTA's slot at the same offset, and writes 128 rows into each CTA's TMEM.  tcgen05.commit
 // with a CTA mask of 0b11 completes ``consumed[s]`` and ``tmem_full[w & 1]`` in both CTAs.
@@ -89,7 +89,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t num_pairs = gridDim.x >> 1;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sA0 = sbase;                        // A of stage s: sA0 + s * kPairStageBytes
-  const uint32_t sB0 = sbase + kABytes;              // B of stage s: sB0 + s * kPairStageBytes
+  const uint32_t sB0 = sbase + kPairABytes;              // B of stage s: sB0 + s * kPairStageBytes
   const uint32_t sEpi = sbase + kPairStages * kPairStageBytes;
 
   const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
@@ -153,7 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                            (half ? sched.part * (kBN / 2) + static_cast<int32_t>(rank) * (kPairBNHalf / 2)
                                  : static_cast<int32_t>(rank) * kPairBNHalf);
         const uint32_t b_chunks = half ? kPairBNHalf / kBChunkCols / 2 : kPairBNHalf / kBChunkCols;
-        const uint32_t tx_bytes = 2u * (kABytes + b_chunks * kBChunkBytes);
+        const uint32_t tx_bytes = 2u * (kPairABytes + b_chunks * kPairBChunkBytes);
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = w * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
@@ -168,9 +168,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
-          const int32_t kx = static_cast<int32_t>(k) * kBK;
+          const int32_t kx = static_cast<int32_t>(k) * kPairBK;
 #pragma unroll
-          for (uint32_t a = 0; a < kKAtoms; ++a) {
+          for (uint32_t a = 0; a < kPairKAtoms; ++a) {
             const uint32_t dst = sA0 + s * kPairStageBytes + a * kAAtomBytes;
             const int32_t ax = kx + static_cast<int32_t>(a * kKAtom);
             if (kAPolicy != 0)
@@ -181,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c) {
             if (c >= b_chunks) break;
-            const uint32_t dst = sB0 + s * kPairStageBytes + c * kBChunkBytes;
+            const uint32_t dst = sB0 + s * kPairStageBytes + c * kPairBChunkBytes;
             const int32_t nx = n0 + static_cast<int32_t>(c * kBChunkCols);
             if (kBPolicy != 0)
               tma_load_2d_pair_hint(dst, &tmB, full_even, nx, kx, pol_b);
@@ -239,11 +239,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = sA0 + s * kPairStageBytes;
           const uint32_t b_addr = sB0 + s * kPairStageBytes;
 #pragma unroll
-          for (uint32_t kk = 0; kk < kBK / kUmmaK; ++kk) {
+          for (uint32_t kk = 0; kk < kPairBK / kUmmaK; ++kk) {
             const uint32_t a_off = (kk / (kKAtom / kUmmaK)) * kAAtomBytes +
                                    (kk % (kKAtom / kUmmaK)) * kUmmaK * kElemBytes;
             const uint64_t a_desc = smem_desc_sw128(a_addr + a_off, 16, 1024);
-            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kBChunkBytes, 1024);
+            const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kPairBChunkBytes, 1024);
             umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
           }
           umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
