@@ -133,26 +133,6 @@ int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uin
   return TG_OK;
 }
 
-// 3-D view of a row-major matrix with 64-element column chunks as the outer dimension:
-// element (x, y, z) = base[y * row_elems + z * 64 + x], x < 64.  Used so that one box covers
-// several 64-column chunks (smem layout chunk-major, exactly as separate 2-D boxes would
-// lay them out).  Only valid when row_elems % 64 == 0 (no chunk runs past a row's end).
-// Returns false (leaving the caller on 2-D boxes) if the driver rejects the map.
-bool encode_3d_chunks(CUtensorMap* map, int dtype, const void* base, uint64_t row_elems,
-                      uint64_t rows, uint32_t box_rows, uint32_t box_chunks) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || row_elems % 64 != 0) return false;
-  const cuuint64_t dims[3] = {64, rows, row_elems / 64};
-  const cuuint64_t strides[2] = {row_elems * tg::kElemBytes, 64 * tg::kElemBytes};
-  const cuuint32_t box[3] = {64, box_rows, box_chunks};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 // Shared validation of the GEMM entry points.  *nothing_to_do is set for M == 0 or N == 0.
@@ -253,16 +233,6 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const int block_k = variant == TG_VARIANT_PAIR ? tg::kPairBK : tg::kBK;
   if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, block_k, "B")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
-  // whole units: one 3-D box per operand and stage when the shape allows it
-  l.tmA3 = l.tmA;
-  l.tmB3 = l.tmB;
-  l.a3d = l.b3d = 0;
-  if (tg::kTma3d) {
-    const int atoms = block_k / tg::kKAtom;
-    const int chunks = (variant == TG_VARIANT_PAIR ? tg::kPairBNHalf : tg::kBN) / tg::kBChunkCols;
-    if (atoms > 1 && encode_3d_chunks(&l.tmA3, dtype, A, K, M, tg::kBM, atoms)) l.a3d = 1;
-    if (chunks > 1 && encode_3d_chunks(&l.tmB3, dtype, B, N, K, block_k, chunks)) l.b3d = 1;
-  }
   l.C = C;
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);

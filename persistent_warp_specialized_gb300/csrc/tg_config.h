@@ -54,12 +54,6 @@ constexpr int kKAtoms = kBK / kKAtom;
 #ifndef TG_EPI_DIRECT
 #define TG_EPI_DIRECT 0
 #endif
-// Whole units load each operand of a stage with one 3-D TMA box (64-column chunks or 64-wide
-// K atoms as the third dimension) when N (for B) or K (for A) is a multiple of 64.
-#ifndef TG_TMA3D
-#define TG_TMA3D 0
-#endif
-constexpr bool kTma3d = TG_TMA3D != 0;
 constexpr int kStages = TG_STAGES;
 constexpr int kAPolicy = TG_A_POLICY;
 constexpr int kBPolicy = TG_B_POLICY;

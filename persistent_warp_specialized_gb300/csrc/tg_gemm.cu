@@ -52,8 +52,6 @@ GemmParams params_of(const GemmLaunch& l) {
   p.k_blocks = l.k_blocks;
   p.group = l.group;
   p.split_from = l.split_from;
-  p.a3d = l.a3d;
-  p.b3d = l.b3d;
   p.total_units = l.total_units;
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
@@ -64,14 +62,14 @@ GemmParams params_of(const GemmLaunch& l) {
 template <int DT, bool DEBUG>
 cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
   gemm_persistent_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, l.tmA3, l.tmB3, params_of(l));
+      l.tmA, l.tmB, l.tmC, params_of(l));
   return cudaGetLastError();
 }
 
 template <int DT, bool DEBUG>
 cudaError_t launch_pair(const GemmLaunch& l, cudaStream_t stream) {
   gemm_pair_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kPairSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, l.tmA3, l.tmB3, params_of(l));
+      l.tmA, l.tmB, l.tmC, params_of(l));
   return cudaGetLastError();
 }
 

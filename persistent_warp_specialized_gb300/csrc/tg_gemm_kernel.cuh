@@ -52,7 +52,6 @@ struct GemmParams {
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;   // tail split of the scheduler (see tg_tile_scheduler.cuh)
-  uint32_t a3d, b3d;                  // 1: tmA3 / tmB3 hold 3-D maps for whole units
   uint64_t watchdog_ns;
   int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
@@ -184,9 +183,7 @@ template <int DT, bool DEBUG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_persistent_ws_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB,
-                              const __grid_constant__ CUtensorMap tmC,
-                              const __grid_constant__ CUtensorMap tmA3,
-                              const __grid_constant__ CUtensorMap tmB3, const GemmParams p) {
+                              const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ GemmCtl ctl;
 
@@ -273,15 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (uint32_t a = 0; a < kKAtoms; ++a)
             load_operand(sA0 + s * kStageBytes + a * kAAtomBytes, &tmA, full,
                          kx + static_cast<int32_t>(a * kKAtom), m0, pol_a, kAPolicy);
-          if (kTma3d && p.b3d && !half) {
-            tma_load_3d(sB0 + s * kStageBytes, &tmB3, full, 0, kx, n0 / kBChunkCols);
-          } else {
 #pragma unroll
-            for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
-              if (c < b_chunks)
-                load_operand(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
-                             n0 + static_cast<int32_t>(c * kBChunkCols), kx, pol_b, kBPolicy);
-          }
+          for (uint32_t c = 0; c < kBN / kBChunkCols; ++c)
+            if (c < b_chunks)
+              load_operand(sB0 + s * kStageBytes + c * kBChunkBytes, &tmB, full,
+                           n0 + static_cast<int32_t>(c * kBChunkCols), kx, pol_b, kBPolicy);
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);
         }

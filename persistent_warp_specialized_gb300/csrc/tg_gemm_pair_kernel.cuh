@@ -78,9 +78,7 @@ template <int DT, bool DEBUG>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_ws_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC,
-                        const __grid_constant__ CUtensorMap tmA3,
-                        const __grid_constant__ CUtensorMap tmB3, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ PairCtl ctl;
 
@@ -171,9 +169,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kPairBK;
-          if (kTma3d && p.a3d) {
-            tma_load_3d_pair(sA0 + s * kPairStageBytes, &tmA3, full_even, 0, m0, kx / kKAtom);
-          } else {
 #pragma unroll
           for (uint32_t a = 0; a < kPairKAtoms; ++a) {
             const uint32_t dst = sA0 + s * kPairStageBytes + a * kAAtomBytes;
@@ -183,10 +178,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             else
               tma_load_2d_pair(dst, &tmA, full_even, ax, m0);
           }
-          }
-          if (kTma3d && p.b3d && !half) {
-            tma_load_3d_pair(sB0 + s * kPairStageBytes, &tmB3, full_even, 0, kx, n0 / kBChunkCols);
-          } else {
 #pragma unroll
           for (uint32_t c = 0; c < kPairBNHalf / kBChunkCols; ++c) {
             if (c >= b_chunks) break;
@@ -196,7 +187,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d_pair_hint(dst, &tmB, full_even, nx, kx, pol_b);
             else
               tma_load_2d_pair(dst, &tmB, full_even, nx, kx);
-          }
           }
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);

@@ -10,12 +10,11 @@
 namespace tg {
 
 struct GemmLaunch {
-  CUtensorMap tmA, tmB, tmC, tmA3, tmB3;
+  CUtensorMap tmA, tmB, tmC;
   void* C;
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;
-  uint32_t a3d, b3d;
   uint32_t grid;
   uint64_t watchdog_ns;
   int32_t* trace;
