@@ -48,7 +48,13 @@ enum {
      the last partial wave of tiles would keep at most half of the workers busy, each of its
      tiles is cut into two half-width (N) units so that wave takes half a tile's time; see
      tg_tile_schedule_ex. */
-  TG_SCHEDULE_PLAIN = 0x100
+  TG_SCHEDULE_PLAIN = 0x100,
+  /* OR'ed into a variant (or into tg_tile_schedule_ex's flags): the scheduler's column_major
+     order -- panels of ``group`` M-tiles with ids running along M first, the grouped decode
+     with the roles of M and N exchanged.  Default: panels of N-tiles, N first, as the page. */
+  TG_SCHEDULE_COLUMN_MAJOR = 0x200,
+  /* tg_tile_schedule_ex flag: apply the tail split (the GEMM does unless TG_SCHEDULE_PLAIN) */
+  TG_SCHEDULE_SPLIT_TAIL = 0x1
 };
 
 /* status codes */
@@ -98,8 +104,9 @@ int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t
 
 /*
  * tg_tile_schedule_ex -- the unit order of the GEMM kernel, with or without the tail split.
- *   split_tail = 0: the rows of tg_tile_schedule, each with part = -1.
- *   split_tail != 0: with T = m_blocks * n_blocks tiles and R = T mod num_sms, if
+ *   flags: TG_SCHEDULE_SPLIT_TAIL and/or TG_SCHEDULE_COLUMN_MAJOR (others: TG_ERR_ARG).
+ *   Without TG_SCHEDULE_SPLIT_TAIL: the rows of tg_tile_schedule, each with part = -1.
+ *   With it: with T = m_blocks * n_blocks tiles and R = T mod num_sms, if
  *     0 < 2R <= num_sms the last R tiles of the grouped order become 2R half-width units:
  *     unit ids 0 .. T-R-1 are whole tiles (part -1), unit T-R+2i+h is half h (0 = left,
  *     1 = right, in N) of tile T-R+i; workers step through unit ids with the grid stride.
@@ -107,7 +114,7 @@ int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t
  *     rows (worker, w, bx, by, part) ordered by worker, then w.
  * Synchronous.  Returns the number of units (rows) or an error.
  */
-int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int split_tail,
+int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int flags,
                         int32_t* out_host);
 
 /* Message of the last failed call on this thread ("" if none). */

@@ -58,6 +58,13 @@ def enumerate_schedule(m_blocks, n_blocks, num_workers, group):
     return rows
 
 
+def tile_coord_column_major(t, m_blocks, n_blocks, group):
+    """The ``column_major`` order of the scheduler: panels of ``group`` M-tiles, ids running
+    along M first, then across N -- the grouped decode with the roles of M and N exchanged."""
+    by, bx = tile_coord(t, n_blocks, m_blocks, group)
+    return bx, by
+
+
 def tail_split_point(m_blocks, n_blocks, num_workers):
     """(F, units): tiles 0..F-1 stay whole; when the last partial wave holds R = T - F tiles
     with 0 < 2R <= P, each of those R tiles becomes two half-width units, else F = T."""
@@ -69,18 +76,19 @@ def tail_split_point(m_blocks, n_blocks, num_workers):
     return first, first + 2 * rem
 
 
-def unit_tile(u, m_blocks, n_blocks, group, first_split):
+def unit_tile(u, m_blocks, n_blocks, group, first_split, column_major=False):
     """Unit id -> (bx, by, part): part -1 is a whole tile, 0 / 1 the left / right half (in N)
     of tile first_split + (u - first_split) // 2."""
+    decode = tile_coord_column_major if column_major else tile_coord
     if u < first_split:
-        bx, by = tile_coord(u, m_blocks, n_blocks, group)
+        bx, by = decode(u, m_blocks, n_blocks, group)
         return bx, by, -1
     t = first_split + (u - first_split) // 2
-    bx, by = tile_coord(t, m_blocks, n_blocks, group)
+    bx, by = decode(t, m_blocks, n_blocks, group)
     return bx, by, (u - first_split) % 2
 
 
-def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True):
+def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True, column_major=False):
     """Rows (worker, w, bx, by, part) of the persistent traversal over work units, ordered
     by worker, then w.  Without the split (or when it does not apply) every unit is a whole
     tile and the rows are those of enumerate_schedule with part = -1.
@@ -99,7 +107,8 @@ def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True):
     for c in range(num_workers):
         w = 0
         while c + w * num_workers < units:
-            bx, by, part = unit_tile(c + w * num_workers, m_blocks, n_blocks, group, first)
+            bx, by, part = unit_tile(c + w * num_workers, m_blocks, n_blocks, group, first,
+                                     column_major)
             rows.append((c, w, bx, by, part))
             w += 1
     return rows

@@ -26,6 +26,8 @@ TG_VARIANT_AUTO = 0
 TG_VARIANT_SINGLE = 1
 TG_VARIANT_PAIR = 2
 TG_SCHEDULE_PLAIN = 0x100
+TG_SCHEDULE_COLUMN_MAJOR = 0x200
+TG_SCHEDULE_SPLIT_TAIL = 0x1
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
@@ -131,25 +133,29 @@ def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
 
 
-def _variant(v, plain=False):
-    """"auto" / "single" / "pair" (or a TG_VARIANT_* int); ``plain`` adds TG_SCHEDULE_PLAIN."""
+def _variant(v, plain=False, column_major=False):
+    """"auto" / "single" / "pair" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
-    return code | (TG_SCHEDULE_PLAIN if plain else 0)
+    return (code | (TG_SCHEDULE_PLAIN if plain else 0)
+            | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0))
 
 
-def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False):
+def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
+                          column_major=False):
     """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
-    ``plain`` walks the page's tile order with no tail split."""
+    ``plain`` walks the page's tile order with no tail split; ``column_major`` the scheduler's
+    column-major order."""
     return _check(load_library().tg_gemm_persistent_ex(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain)))
+        _variant(variant, plain, column_major)))
 
 
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
-                             watchdog_ns=0, inject_skip_phase=-1, plain=False):
+                             watchdog_ns=0, inject_skip_phase=-1, plain=False,
+                             column_major=False):
     return _check(load_library().tg_gemm_persistent_debug(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain), _ptr(trace), watchdog_ns, inject_skip_phase))
+        _variant(variant, plain, column_major), _ptr(trace), watchdog_ns, inject_skip_phase))
 
 
 def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,
@@ -188,12 +194,13 @@ def tg_tile_schedule(m_blocks, n_blocks, num_sms, group):
     return [tuple(buf[4 * i: 4 * i + 4]) for i in range(n)]
 
 
-def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True):
+def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True, column_major=False):
     """Rows (worker, w, bx, by, part) of the device scheduler over work units."""
     rows = 2 * max(0, m_blocks) * max(0, n_blocks)
     buf = (ctypes.c_int32 * (5 * max(rows, 1)))()
-    n = _check(load_library().tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group,
-                                                  1 if split_tail else 0, buf))
+    flags = (TG_SCHEDULE_SPLIT_TAIL if split_tail else 0) | (
+        TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
+    n = _check(load_library().tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, flags, buf))
     return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
 
 

@@ -204,8 +204,10 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
   return sh;
 }
 
+constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR;
+
 bool known_variant(int v) {
-  const int kernel = v & ~TG_SCHEDULE_PLAIN;
+  const int kernel = v & ~kScheduleFlags;
   return kernel == TG_VARIANT_AUTO || kernel == TG_VARIANT_SINGLE || kernel == TG_VARIANT_PAIR;
 }
 
@@ -214,7 +216,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
               int64_t inject) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
-  variant &= ~TG_SCHEDULE_PLAIN;
+  const uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
+  variant &= ~kScheduleFlags;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
   if (rc != TG_OK || nothing) return rc;
@@ -242,6 +245,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.n_blocks = sh.n_tiles;
   l.split_from = sh.split_from;
   l.total_units = sh.units;
+  l.column_major = column_major;
   l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
   l.group = tg::kGroup;
   l.grid = sh.ctas;
@@ -284,7 +288,7 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
                          int* ctas, int* split_from, int* units) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
-  variant &= ~TG_SCHEDULE_PLAIN;
+  variant &= ~kScheduleFlags;
   if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
   int sms = 0, max_pairs = 0;
@@ -318,12 +322,13 @@ int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, 
 // Runs the device scheduler over [0, units) and copies rows of ``width`` int32 (4: without
 // the part column, 5: with it) to the host.
 int schedule_rows(int m_blocks, int n_blocks, int num_sms, int group, uint32_t split_from,
-                  uint32_t units, int width, int32_t* out_host) {
+                  uint32_t units, uint32_t column_major, int width, int32_t* out_host) {
   const uint64_t rows = units;
   int32_t* d = nullptr;
   cudaError_t e = cudaMalloc(&d, rows * 5 * sizeof(int32_t));
   if (e != cudaSuccess) return fail_cuda("cudaMalloc", e);
-  e = tg::launch_tile_schedule(m_blocks, n_blocks, num_sms, group, split_from, units, d, nullptr);
+  e = tg::launch_tile_schedule(m_blocks, n_blocks, num_sms, group, split_from, units,
+                               column_major, d, nullptr);
   if (e == cudaSuccess) {
     if (width == 5) {
       e = cudaMemcpy(out_host, d, rows * 5 * sizeof(int32_t), cudaMemcpyDeviceToHost);
@@ -350,17 +355,21 @@ int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t
   int rc = check_schedule_args(m_blocks, n_blocks, num_sms, group, out_host);
   if (rc != TG_OK) return rc;
   const uint32_t tiles = uint32_t(m_blocks) * uint32_t(n_blocks);
-  return schedule_rows(m_blocks, n_blocks, num_sms, group, tiles, tiles, 4, out_host);
+  return schedule_rows(m_blocks, n_blocks, num_sms, group, tiles, tiles, 0, 4, out_host);
 }
 
-int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int split_tail,
+int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int flags,
                         int32_t* out_host) {
   int rc = check_schedule_args(m_blocks, n_blocks, num_sms, group, out_host);
   if (rc != TG_OK) return rc;
+  if (flags & ~(TG_SCHEDULE_SPLIT_TAIL | TG_SCHEDULE_COLUMN_MAJOR))
+    return fail(TG_ERR_ARG, "unknown schedule flags 0x%x", flags);
   const uint32_t tiles = uint32_t(m_blocks) * uint32_t(n_blocks);
   uint32_t first = tiles, units = tiles;
-  if (split_tail) tg::PersistentTileScheduler::tail_split(tiles, uint32_t(num_sms), first, units);
-  return schedule_rows(m_blocks, n_blocks, num_sms, group, first, units, 5, out_host);
+  if (flags & TG_SCHEDULE_SPLIT_TAIL)
+    tg::PersistentTileScheduler::tail_split(tiles, uint32_t(num_sms), first, units);
+  return schedule_rows(m_blocks, n_blocks, num_sms, group, first, units,
+                       (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u, 5, out_host);
 }
 
 const char* tg_last_error(void) { return g_err; }

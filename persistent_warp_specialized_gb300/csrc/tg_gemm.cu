@@ -14,13 +14,14 @@ namespace {
 // q + (c < r) tiles where total = q * P + r, so its first row is c * q + min(c, r).
 __global__ void tile_schedule_kernel(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
                                      uint32_t group, uint32_t split_from, uint32_t units,
-                                     int32_t* __restrict__ out) {
+                                     uint32_t column_major, int32_t* __restrict__ out) {
   const uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= num_workers) return;
   const uint32_t q = units / num_workers;
   const uint32_t r = units % num_workers;
   uint64_t row = static_cast<uint64_t>(c) * q + (c < r ? c : r);
-  PersistentTileScheduler sched(m_blocks, n_blocks, group, num_workers, split_from, units);
+  PersistentTileScheduler sched(m_blocks, n_blocks, group, num_workers, split_from, units,
+                                column_major);
   sched.init(c);
   while (sched.valid()) {
     int32_t* o = out + 5 * row;
@@ -52,6 +53,7 @@ GemmParams params_of(const GemmLaunch& l) {
   p.k_blocks = l.k_blocks;
   p.group = l.group;
   p.split_from = l.split_from;
+  p.column_major = l.column_major;
   p.total_units = l.total_units;
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
@@ -132,11 +134,11 @@ cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {
 
 cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
                                  uint32_t group, uint32_t split_from, uint32_t units,
-                                 int32_t* out_dev, cudaStream_t stream) {
+                                 uint32_t column_major, int32_t* out_dev, cudaStream_t stream) {
   const uint32_t threads = 128;
   const uint32_t blocks = (num_workers + threads - 1) / threads;
   tile_schedule_kernel<<<blocks, threads, 0, stream>>>(m_blocks, n_blocks, num_workers, group,
-                                                       split_from, units, out_dev);
+                                                       split_from, units, column_major, out_dev);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,7 @@ struct GemmParams {
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;   // tail split of the scheduler (see tg_tile_scheduler.cuh)
+  uint32_t column_major;              // scheduler order option
   uint64_t watchdog_ns;
   int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
       sched.init(blockIdx.x);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_full = idesc_f16(DT, kBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
       constexpr uint32_t idesc_half = idesc_f16(DT, kBM, kBN / 2, 0, 1);
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
       sched.init(blockIdx.x);
       bool ok = true;
       while (ok && sched.valid()) {
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp - kFirstEpiWarp;       // TMEM lanes 32q .. 32q + 31
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
     sched.init(blockIdx.x);
     uint32_t chunk = 0;
     while (sched.valid()) {

@@ -137,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
       sched.init(pair);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
@@ -212,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_full = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
       constexpr uint32_t idesc_half = idesc_f16(DT, kPairBM, kBN / 2, 0, 1);
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
       sched.init(pair);
       bool ok = true;
       while (ok && sched.valid()) {
@@ -260,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t q = warp - kFirstEpiWarp;
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units);
+                                    p.total_units, p.column_major);
     sched.init(pair);
     uint32_t chunk = 0;
     while (sched.valid()) {

@@ -15,6 +15,7 @@ struct GemmLaunch {
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;
+  uint32_t column_major;
   uint32_t grid;
   uint64_t watchdog_ns;
   int32_t* trace;
@@ -37,7 +38,7 @@ cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream);
 // split_from are whole (part -1)
 cudaError_t launch_tile_schedule(uint32_t m_blocks, uint32_t n_blocks, uint32_t num_workers,
                                  uint32_t group, uint32_t split_from, uint32_t units,
-                                 int32_t* out_dev, cudaStream_t stream);
+                                 uint32_t column_major, int32_t* out_dev, cudaStream_t stream);
 cudaError_t clear_watchdog_status(cudaStream_t stream);
 // synchronises ``stream``, returns the status word in *out and clears it
 cudaError_t read_and_clear_watchdog_status(unsigned int* out, cudaStream_t stream);

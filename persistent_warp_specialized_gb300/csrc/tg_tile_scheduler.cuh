@@ -25,6 +25,9 @@
 // each cut into two half-width units (part 0 = left, part 1 = right half in N), numbered
 // split_from + 2 (t - split_from) + part, so that wave takes half a tile's time.  Without a
 // split, split_from = total_units = T and every unit is the page's tile (part = -1).
+//
+// column_major (the page's scheduler option of that name): panels of g M-tiles with ids running
+// along M first -- the same decode with the roles of (m_blocks, bx) and (n_blocks, by) swapped.
 #pragma once
 
 #include <cstdint>
@@ -39,15 +42,18 @@ struct PersistentTileScheduler {
   uint32_t linear_idx;    // worker + w * num_workers
   uint32_t m_idx, n_idx;  // decoded tile (valid only while valid())
   int32_t part;           // -1 whole tile, 0 / 1 left / right half in N
+  uint32_t column_major;  // 1: panels of g M-tiles, M fastest
 
   // the page's traversal: every unit a whole tile
   __host__ __device__ PersistentTileScheduler(uint32_t m, uint32_t n, uint32_t g, uint32_t p)
-      : PersistentTileScheduler(m, n, g, p, m * n, m * n) {}
+      : PersistentTileScheduler(m, n, g, p, m * n, m * n, 0) {}
 
   __host__ __device__ PersistentTileScheduler(uint32_t m, uint32_t n, uint32_t g, uint32_t p,
-                                              uint32_t first_split, uint32_t units)
+                                              uint32_t first_split, uint32_t units,
+                                              uint32_t col_major)
       : m_blocks(m), n_blocks(n), group(g), num_workers(p), split_from(first_split),
-        total_units(units), current_iter(0), linear_idx(0), m_idx(0), n_idx(0), part(-1) {}
+        total_units(units), current_iter(0), linear_idx(0), m_idx(0), n_idx(0), part(-1),
+        column_major(col_major) {}
 
   // (split_from, total_units) for T tiles over P workers: split the last partial wave when
   // it holds R tiles with 0 < 2R <= P.
@@ -74,14 +80,21 @@ struct PersistentTileScheduler {
     by = first_col + u % width;
   }
 
+  __host__ __device__ void decode_tile(uint32_t t) {
+    if (column_major)
+      coord(t, n_blocks, m_blocks, group, n_idx, m_idx);
+    else
+      coord(t, m_blocks, n_blocks, group, m_idx, n_idx);
+  }
+
   __host__ __device__ void decode() {
     if (linear_idx >= total_units) return;
     if (linear_idx < split_from) {
-      coord(linear_idx, m_blocks, n_blocks, group, m_idx, n_idx);
+      decode_tile(linear_idx);
       part = -1;
     } else {
       const uint32_t v = linear_idx - split_from;
-      coord(split_from + v / 2, m_blocks, n_blocks, group, m_idx, n_idx);
+      decode_tile(split_from + v / 2);
       part = static_cast<int32_t>(v & 1u);
     }
   }

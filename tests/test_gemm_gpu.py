@@ -112,6 +112,19 @@ def test_split_tail_after_full_waves_is_bit_exact(variant, plain):
     assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_column_major_order_is_bit_exact(variant):
+    M, N, K = 3000, 2304, 320
+    a, b = wl.small_int_inputs(M, N, K, "f16", seed=13)
+    a_d, b_d = a.cuda(), b.cuda()
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_persistent_ex(a_d, b_d, c, M, N, K, "f16", variant=variant, column_major=True)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "f16"))
+
+
 def test_k_zero_gives_zeros():
     c = torch.full((64, 64), 7.0, dtype=torch.bfloat16, device="cuda")
     a = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")

@@ -149,3 +149,38 @@ def test_split_units_follow_the_grid_stride_and_the_grouped_order():
     # workers' unit counts differ by at most one
     counts = [sum(1 for r in rows if r[0] == c) for c in range(p)]
     assert max(counts) - min(counts) <= 1
+
+
+@pytest.mark.parametrize("group", [1, 2, 3, 8, 16])
+def test_column_major_every_tile_exactly_once(group):
+    for m, n in GRIDS:
+        seen = [schedule.tile_coord_column_major(t, m, n, group) for t in range(m * n)]
+        assert sorted(seen) == [(bx, by) for bx in range(m) for by in range(n)], (m, n, group)
+
+
+def test_column_major_textbook_orders():
+    for m, n in GRIDS:
+        for t in range(m * n):
+            # group 1: row-major walk of the tile grid; one panel (group >= m): column-major
+            assert schedule.tile_coord_column_major(t, m, n, 1) == (t // n, t % n)
+            assert schedule.tile_coord_column_major(t, m, n, m) == (t % m, t // m)
+
+
+def test_column_major_panels_top_to_bottom():
+    m, n, g = 13, 9, 4
+    coords = [schedule.tile_coord_column_major(t, m, n, g) for t in range(m * n)]
+    panels = [bx // g for bx, _ in coords]
+    assert panels == sorted(panels)
+    # inside a panel, ids run down M first: g consecutive ids share by
+    assert coords[:4] == [(0, 0), (1, 0), (2, 0), (3, 0)]
+    assert coords[4] == (0, 1)
+
+
+def test_column_major_units_cover_every_tile():
+    for m, n, p in [(32, 28, 76), (5, 9, 7), (64, 32, 152)]:
+        rows = schedule.enumerate_units(m, n, p, 8, split_tail=True, column_major=True)
+        cover = {}
+        for (_, _, bx, by, part) in rows:
+            cover.setdefault((bx, by), []).append(part)
+        assert sorted(cover) == [(x, y) for x in range(m) for y in range(n)]
+        assert all(sorted(v) in ([-1], [0, 1]) for v in cover.values())

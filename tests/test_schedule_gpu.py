@@ -48,9 +48,10 @@ def test_schedule_matches_stored_fixture(name):
 def test_unit_schedule_brute_force_grids():
     for m, n, g, p in itertools.product([1, 2, 5, 8, 13, 32, 64], [1, 3, 4, 9, 16, 28, 32],
                                         [1, 8], [1, 7, 76, 148, 152]):
-        for split in (False, True):
-            got = tg.tg_tile_schedule_ex(m, n, p, g, split)
-            assert got == schedule.enumerate_units(m, n, p, g, split), (m, n, g, p, split)
+        for split, cm in itertools.product((False, True), (False, True)):
+            got = tg.tg_tile_schedule_ex(m, n, p, g, split, cm)
+            want = schedule.enumerate_units(m, n, p, g, split, cm)
+            assert got == want, (m, n, g, p, split, cm)
 
 
 def test_config1_schedule_148_workers():
@@ -59,11 +60,11 @@ def test_config1_schedule_148_workers():
         (0, 0, 0, 0), (1, 0, 1, 0)]
 
 
-@pytest.mark.parametrize("plain", [False, True])
+@pytest.mark.parametrize("plain,column_major", [(False, False), (True, False), (False, True)])
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(4000, 7000, 256), (8192, 8192, 64), (1024, 1024, 1024),
                                    (256, 256, 256), (4000, 2048, 128), (2560, 2560, 128)])
-def test_kernel_followed_the_schedule(M, N, K, variant, plain):
+def test_kernel_followed_the_schedule(M, N, K, variant, plain, column_major):
     # the epilogue of the real GEMM records (worker, w, bx, by, part) for every unit it stored
     shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
     m_tiles, n_tiles, workers = shape["m_tiles"], shape["n_tiles"], shape["workers"]
@@ -73,9 +74,9 @@ def test_kernel_followed_the_schedule(M, N, K, variant, plain):
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
     assert tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
-                                       trace=trace, plain=plain) == 0
+                                       trace=trace, plain=plain, column_major=column_major) == 0
     want = schedule.enumerate_units(m_tiles, n_tiles, workers, tg.tg_gemm_config()["group"],
-                                    split_tail=not plain)
+                                    split_tail=not plain, column_major=column_major)
     assert len(want) == units
     by_unit = {}
     for (worker, w, bx, by, part) in want:
