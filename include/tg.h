@@ -53,6 +53,12 @@ enum {
      order -- panels of ``group`` M-tiles with ids running along M first, the grouped decode
      with the roles of M and N exchanged.  Default: panels of N-tiles, N first, as the page. */
   TG_SCHEDULE_COLUMN_MAJOR = 0x200,
+  /* OR'ed into TG_VARIANT_SINGLE: dynamic persistence.  One CTA is launched per work unit; the
+     ~#SMs that run first keep going and take over the units of CTAs not yet launched by
+     cancelling those launches (cluster launch control, clusterlaunchcontrol.try_cancel), so
+     units go to whichever SM frees up first.  The unit-to-CTA assignment is then decided at run
+     time (the debug trace records it); the set of units and their decode are unchanged. */
+  TG_SCHEDULE_DYNAMIC = 0x400,
   /* tg_tile_schedule_ex flag: apply the tail split (the GEMM does unless TG_SCHEDULE_PLAIN) */
   TG_SCHEDULE_SPLIT_TAIL = 0x1
 };

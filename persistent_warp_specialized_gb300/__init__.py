@@ -28,6 +28,7 @@ TG_VARIANT_PAIR = 2
 TG_SCHEDULE_PLAIN = 0x100
 TG_SCHEDULE_COLUMN_MAJOR = 0x200
 TG_SCHEDULE_SPLIT_TAIL = 0x1
+TG_SCHEDULE_DYNAMIC = 0x400
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
@@ -133,29 +134,31 @@ def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
 
 
-def _variant(v, plain=False, column_major=False):
+def _variant(v, plain=False, column_major=False, dynamic=False):
     """"auto" / "single" / "pair" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
     return (code | (TG_SCHEDULE_PLAIN if plain else 0)
-            | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0))
+            | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
+            | (TG_SCHEDULE_DYNAMIC if dynamic else 0))
 
 
 def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
-                          column_major=False):
+                          column_major=False, dynamic=False):
     """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
     ``plain`` walks the page's tile order with no tail split; ``column_major`` the scheduler's
     column-major order."""
     return _check(load_library().tg_gemm_persistent_ex(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major)))
+        _variant(variant, plain, column_major, dynamic)))
 
 
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
                              watchdog_ns=0, inject_skip_phase=-1, plain=False,
-                             column_major=False):
+                             column_major=False, dynamic=False):
     return _check(load_library().tg_gemm_persistent_debug(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major), _ptr(trace), watchdog_ns, inject_skip_phase))
+        _variant(variant, plain, column_major, dynamic), _ptr(trace), watchdog_ns,
+        inject_skip_phase))
 
 
 def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,
@@ -176,10 +179,10 @@ def tg_gemm_config():
     return dict(zip(keys, (v.value for v in vals)))
 
 
-def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False):
+def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False, dynamic=False):
     """The persistent launch the library uses for M x N x K on the current device."""
     vals = [ctypes.c_int() for _ in range(9)]
-    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant, plain),
+    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant, plain, False, dynamic),
                                                *[ctypes.byref(v) for v in vals]))
     keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas",
             "split_from", "units")

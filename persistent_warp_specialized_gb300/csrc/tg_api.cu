@@ -185,8 +185,8 @@ struct Shape {
 // Persistent launch of a concrete variant: one worker per SM (SINGLE) or per resident CTA
 // pair (PAIR), never more workers than work units; the last partial wave is split into
 // half-width units unless ``plain`` (the page's traversal) is asked for.
-Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain, int sms,
-                   int max_pairs) {
+Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain, bool dynamic,
+                   int sms, int max_pairs) {
   Shape sh;
   sh.tile_m = variant == TG_VARIANT_PAIR ? tg::kPairBM : tg::kBM;
   sh.tile_n = tg::kBN;
@@ -199,12 +199,14 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
   } else {
     tg::PersistentTileScheduler::tail_split(tiles, slots, sh.split_from, sh.units);
   }
-  sh.workers = sh.units < slots ? sh.units : slots;
+  // dynamic persistence launches one CTA per unit; only ~#SMs run at once and they take over
+  // the rest through cluster launch control
+  sh.workers = dynamic ? sh.units : (sh.units < slots ? sh.units : slots);
   sh.ctas = variant == TG_VARIANT_PAIR ? 2 * sh.workers : sh.workers;
   return sh;
 }
 
-constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR;
+constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | TG_SCHEDULE_DYNAMIC;
 
 bool known_variant(int v) {
   const int kernel = v & ~kScheduleFlags;
@@ -217,6 +219,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   const uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
+  const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
   variant &= ~kScheduleFlags;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
@@ -226,6 +229,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
   if (variant == TG_VARIANT_PAIR && max_pairs < 1)
     return fail(TG_ERR_CUDA, "no CTA pair of the pair kernel fits on this device");
+  if (dynamic && variant != TG_VARIANT_SINGLE)
+    return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) {
     cudaError_t e = tg::launch_zero_fill(C, uint64_t(M) * N * tg::kElemBytes, s);
@@ -240,12 +245,13 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
-  const Shape sh = launch_shape(M, N, K, variant, plain, sms, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
   l.m_blocks = sh.m_tiles;
   l.n_blocks = sh.n_tiles;
   l.split_from = sh.split_from;
   l.total_units = sh.units;
   l.column_major = column_major;
+  l.dynamic = dynamic ? 1u : 0u;
   l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
   l.group = tg::kGroup;
   l.grid = sh.ctas;
@@ -288,6 +294,7 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
                          int* ctas, int* split_from, int* units) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
+  const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
   variant &= ~kScheduleFlags;
   if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
@@ -295,7 +302,9 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
   int rc = device_ready(&sms, &max_pairs);
   if (rc != TG_OK) return rc;
   if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
-  const Shape sh = launch_shape(M, N, K, variant, plain, sms, max_pairs);
+  if (dynamic && variant != TG_VARIANT_SINGLE)
+    return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
+  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
   if (variant_out) *variant_out = variant;
   if (tile_m) *tile_m = static_cast<int>(sh.tile_m);
   if (tile_n) *tile_n = static_cast<int>(sh.tile_n);

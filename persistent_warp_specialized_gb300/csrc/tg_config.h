@@ -118,6 +118,11 @@ constexpr uint32_t kRoleProducer = 1u;
 constexpr uint32_t kRoleMma = 2u;
 constexpr uint32_t kRoleEpilogue = 4u;
 constexpr uint32_t kRoleDrain = 8u;
+constexpr uint32_t kRoleSched = 16u;
+// dynamic persistence: try_cancel responses kept in flight, and the threads that read each
+// (producer thread, MMA thread, one lane per epilogue warp)
+constexpr int kSchedSlots = 2;
+constexpr uint32_t kSchedConsumers = 2 + kEpiWarps;
 constexpr uint64_t kDefaultWatchdogNs = 1ull << 32;  // about 4.3 s
 
 }  // namespace tg

@@ -53,6 +53,7 @@ struct GemmParams {
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;   // tail split of the scheduler (see tg_tile_scheduler.cuh)
   uint32_t column_major;              // scheduler order option
+  uint32_t dynamic;                   // 1: units handed out by cluster launch control
   uint64_t watchdog_ns;
   int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
@@ -61,7 +62,10 @@ struct GemmParams {
 // Per-device status word of the watchdog (bits: kRole*).  Read and cleared by the host.
 __device__ unsigned int g_watchdog_status = 0;
 
-struct __align__(8) GemmCtl {
+struct __align__(16) GemmCtl {
+  uint4 sched_resp[kSchedSlots];      // cluster-launch-control responses (dynamic mode)
+  uint64_t sched_full[kSchedSlots];
+  uint64_t sched_empty[kSchedSlots];
   uint64_t loaded[kStages];
   uint64_t consumed[kStages];
   uint64_t tmem_full[2];
@@ -170,6 +174,39 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], ui
   __syncwarp();   // converged for the next warp-collective tcgen05.ld
 }
 
+// Dynamic persistence (cluster launch control).  The grid holds one CTA per work unit; a CTA
+// first runs the unit of its own index, then takes over the units of CTAs that have not been
+// launched yet: warp 3 asks the hardware to cancel one pending CTA at a time
+// (clusterlaunchcontrol.try_cancel) into a ring of kSchedSlots responses; the response for a
+// CTA's iteration w (w >= 1) sits in slot w % kSchedSlots, completed on sched_full; each of
+// the kSchedConsumers readers arrives on sched_empty once it has read it.  A response that
+// cancelled nothing ends the CTA's traversal.
+enum ClcNext : int { kClcUnit = 0, kClcDone = 1, kClcAbort = 2 };
+
+__device__ __forceinline__ int clc_next_unit(PersistentTileScheduler& sched, uint32_t w,
+                                             uint32_t resp0, uint32_t full0, uint32_t empty0,
+                                             volatile int* abort_flag, uint64_t limit,
+                                             uint32_t role, bool warp_wide, bool arrive) {
+  const uint32_t slot = w % kSchedSlots;
+  const uint32_t par = (w / kSchedSlots) & 1u;
+  bool got = wait_or_abort(full0 + 8u * slot, par, abort_flag, limit, role);
+  if (warp_wide) got = __all_sync(0xffffffffu, got);
+  if (!got) {
+    sched.finish();
+    return kClcAbort;
+  }
+  uint32_t unit = 0;
+  const bool cancelled = clc_response(resp0 + 16u * slot, &unit);
+  if (warp_wide) __syncwarp();
+  if (arrive) mbar_arrive(empty0 + 8u * slot);
+  if (!cancelled) {
+    sched.finish();
+    return kClcDone;
+  }
+  sched.jump(unit, w);
+  return kClcUnit;
+}
+
 // A and B loads of one k-block slot, with the configured L2 policies.
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                              int32_t x, int32_t y, uint64_t policy, int kind) {
@@ -200,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tmem_full = smem_u32(&ctl.tmem_full[0]);
   const uint32_t bar_tmem_empty = smem_u32(&ctl.tmem_empty[0]);
   const uint32_t bar_drain = smem_u32(&ctl.drain);
+  const uint32_t sched_resp0 = smem_u32(&ctl.sched_resp[0]);
+  const uint32_t sched_full0 = smem_u32(&ctl.sched_full[0]);
+  const uint32_t sched_empty0 = smem_u32(&ctl.sched_empty[0]);
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -213,6 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tmem_empty + 8u * b, kEpiThreads);
     }
     mbar_init(bar_drain, 1);
+#pragma unroll
+    for (int i = 0; i < kSchedSlots; ++i) {
+      mbar_init(sched_full0 + 8u * i, 1);
+      mbar_init(sched_empty0 + 8u * i, kSchedConsumers);
+    }
     ctl.abort = 0;
     fence_mbarrier_init();
   }
@@ -279,7 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending |= 1u << s;
           pending_par = (pending_par & ~(1u << s)) | (par << s);
         }
-        sched.next_tile();
+        if (p.dynamic) {
+          if (clc_next_unit(sched, static_cast<uint32_t>(w) + 1, sched_resp0, sched_full0, sched_empty0,
+                            abort_flag, limit, kRoleProducer, false, true) == kClcAbort)
+            ok = false;
+        } else {
+          sched.next_tile();
+        }
       }
       if (!ok) {
         for (uint32_t s = 0; s < kStages; ++s)
@@ -335,11 +386,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         umma_commit(bar_tmem_full + 8u * buf);
-        sched.next_tile();
+        if (p.dynamic) {
+          if (clc_next_unit(sched, w + 1, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
+                            kRoleMma, false, true) == kClcAbort)
+            ok = false;
+        } else {
+          sched.next_tile();
+        }
       }
       // every MMA this thread issued has finished before TMEM can be released
       umma_commit(bar_drain);
       wait_bounded(bar_drain, 0, limit, kRoleDrain);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ unit fetcher (dynamic mode)
+    if (lane == 0 && p.dynamic) {
+      for (uint32_t i = 1;; ++i) {   // the response for iteration i of this CTA
+        const uint32_t slot = i % kSchedSlots;
+        const uint32_t par = (i / kSchedSlots) & 1u;
+        if (!wait_or_abort(sched_empty0 + 8u * slot, par ^ 1u, abort_flag, limit, kRoleSched))
+          break;
+        mbar_arrive_expect_tx(sched_full0 + 8u * slot, 16);
+        clc_try_cancel(sched_resp0 + 16u * slot, sched_full0 + 8u * slot);
+        if (!wait_or_abort(sched_full0 + 8u * slot, par, abort_flag, limit, kRoleSched)) {
+          wait_bounded(sched_full0 + 8u * slot, par, limit, kRoleDrain);  // let it land
+          break;
+        }
+        uint32_t unit;
+        if (!clc_response(sched_resp0 + 16u * slot, &unit)) break;   // nothing left to take
+      }
     }
     __syncwarp();
   } else if (warp >= kFirstEpiWarp) {
@@ -382,7 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr[3] = static_cast<int32_t>(sched.n_idx);
         tr[4] = sched.part;
       }
-      sched.next_tile();
+      if (p.dynamic) {
+        if (clc_next_unit(sched, w + 1, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
+                          kRoleEpilogue, true, lane == 0) == kClcAbort)
+          break;
+      } else {
+        sched.next_tile();
+      }
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();

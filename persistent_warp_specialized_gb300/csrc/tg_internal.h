@@ -16,6 +16,7 @@ struct GemmLaunch {
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;
   uint32_t column_major;
+  uint32_t dynamic;
   uint32_t grid;
   uint64_t watchdog_ns;
   int32_t* trace;

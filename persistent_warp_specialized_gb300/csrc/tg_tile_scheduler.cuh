@@ -112,6 +112,16 @@ struct PersistentTileScheduler {
     linear_idx += num_workers;
     decode();
   }
+
+  // dynamic persistence: the w-th unit of this worker is ``unit`` (handed out at run time)
+  __host__ __device__ void jump(uint32_t unit, uint32_t w) {
+    current_iter = w;
+    linear_idx = unit;
+    decode();
+  }
+
+  // no further unit for this worker
+  __host__ __device__ void finish() { linear_idx = total_units; }
 };
 
 }  // namespace tg
