@@ -27,8 +27,13 @@ What it computes, and where the pages define it
   #2441", the removed ``for w in T.unroll(waves)`` form, and the
   ``PersistentTileScheduler(..., swizzle_size=group_size)`` that replaces it).
 
+* ``mx``       -- the block-scaled MXFP8 GEMM of the same PR
+  (examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py): E4M3 elements, one
+  E8M0 scale per 32 K-elements of each A row and each B column, exact scaled products,
+  binary64 sum, one rounding to the output type.
+
 Pins (tests that tie the oracle to something other than itself): see
-``tests/test_oracle_formats.py``, ``tests/test_oracle_gemm.py`` and
-``tests/test_oracle_schedule.py``.  Every function here is pinned; none is
+``tests/test_oracle_formats.py``, ``tests/test_oracle_gemm.py``,
+``tests/test_oracle_schedule.py`` and ``tests/test_oracle_mx.py``.  Every function here is pinned; none is
 "parity unpinned".
 """
