@@ -177,18 +177,20 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], ui
 // Dynamic persistence (cluster launch control).  The grid holds one CTA per work unit; a CTA
 // first runs the unit of its own index, then takes over the units of CTAs that have not been
 // launched yet: warp 3 asks the hardware to cancel one pending CTA at a time
-// (clusterlaunchcontrol.try_cancel) into a ring of kSchedSlots responses; the response for a
-// CTA's iteration w (w >= 1) sits in slot w % kSchedSlots, completed on sched_full; each of
-// the kSchedConsumers readers arrives on sched_empty once it has read it.  A response that
-// cancelled nothing ends the CTA's traversal.
+// (clusterlaunchcontrol.try_cancel) into a ring of kSchedSlots responses.  Fetch j (0-based:
+// the unit that follows the CTA's iteration j) sits in slot j % kSchedSlots, the (j /
+// kSchedSlots)-th use of that slot, completed on sched_full; each of the kSchedConsumers
+// readers arrives on sched_empty once it has read it.  A response that cancelled nothing ends
+// the CTA's traversal.
 enum ClcNext : int { kClcUnit = 0, kClcDone = 1, kClcAbort = 2 };
 
-__device__ __forceinline__ int clc_next_unit(PersistentTileScheduler& sched, uint32_t w,
+// ``j``: the iteration just finished (the fetch index); the next unit becomes iteration j + 1.
+__device__ __forceinline__ int clc_next_unit(PersistentTileScheduler& sched, uint32_t j,
                                              uint32_t resp0, uint32_t full0, uint32_t empty0,
                                              volatile int* abort_flag, uint64_t limit,
                                              uint32_t role, bool warp_wide, bool arrive) {
-  const uint32_t slot = w % kSchedSlots;
-  const uint32_t par = (w / kSchedSlots) & 1u;
+  const uint32_t slot = j % kSchedSlots;
+  const uint32_t par = (j / kSchedSlots) & 1u;
   bool got = wait_or_abort(full0 + 8u * slot, par, abort_flag, limit, role);
   if (warp_wide) got = __all_sync(0xffffffffu, got);
   if (!got) {
@@ -203,7 +205,7 @@ __device__ __forceinline__ int clc_next_unit(PersistentTileScheduler& sched, uin
     sched.finish();
     return kClcDone;
   }
-  sched.jump(unit, w);
+  sched.jump(unit, j + 1);
   return kClcUnit;
 }
 
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending_par = (pending_par & ~(1u << s)) | (par << s);
         }
         if (p.dynamic) {
-          if (clc_next_unit(sched, static_cast<uint32_t>(w) + 1, sched_resp0, sched_full0, sched_empty0,
+          if (clc_next_unit(sched, static_cast<uint32_t>(w), sched_resp0, sched_full0, sched_empty0,
                             abort_flag, limit, kRoleProducer, false, true) == kClcAbort)
             ok = false;
         } else {
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         umma_commit(bar_tmem_full + 8u * buf);
         if (p.dynamic) {
-          if (clc_next_unit(sched, w + 1, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
+          if (clc_next_unit(sched, w, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
                             kRoleMma, false, true) == kClcAbort)
             ok = false;
         } else {
@@ -402,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 3) {
     // ------------------------------------------------------------ unit fetcher (dynamic mode)
     if (lane == 0 && p.dynamic) {
-      for (uint32_t i = 1;; ++i) {   // the response for iteration i of this CTA
-        const uint32_t slot = i % kSchedSlots;
-        const uint32_t par = (i / kSchedSlots) & 1u;
+      for (uint32_t j = 0;; ++j) {   // fetch j: the unit of this CTA's iteration j + 1
+        const uint32_t slot = j % kSchedSlots;
+        const uint32_t par = (j / kSchedSlots) & 1u;
         if (!wait_or_abort(sched_empty0 + 8u * slot, par ^ 1u, abort_flag, limit, kRoleSched))
           break;
         mbar_arrive_expect_tx(sched_full0 + 8u * slot, 16);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr[4] = sched.part;
       }
       if (p.dynamic) {
-        if (clc_next_unit(sched, w + 1, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
+        if (clc_next_unit(sched, w, sched_resp0, sched_full0, sched_empty0, abort_flag, limit,
                           kRoleEpilogue, true, lane == 0) == kClcAbort)
           break;
       } else {

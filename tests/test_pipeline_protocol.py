@@ -145,3 +145,106 @@ def test_parities_match_the_generated_sm90_pipeline():
         assert slot_of(k, 3) == k % 3
         assert parity_of(k, 3) == (k % 6) // 3
         assert parity_of(k, 3) ^ 1 == ((k % 6) // 3) ^ 1
+
+
+# ---------------------------------------------------------------- unit-response ring
+# Dynamic persistence: warp 3 fetches units by cancelling pending CTAs into a ring of
+# ``slots`` 16-byte responses.  Fetch j (the unit after the CTA's iteration j) lands in slot
+# ``j % slots`` and completes ``full[slot]``; each of ``consumers`` readers (producer, MMA,
+# four epilogue warps) reads it after waiting ``full[slot]`` with parity
+# ``(j // slots) & 1`` and arrives on ``empty[slot]`` (arrival count ``consumers``); the
+# fetcher waits ``empty[slot]`` with parity ``((j // slots) & 1) ^ 1`` before reusing it.
+# A response that cancelled nothing (``None``) ends the traversal of every role.
+# ``first`` shifts the fetch numbering: the kernel once numbered fetches from 1, so the
+# first use of slot 0 waited on parity 1, which a fresh barrier passes at once.
+
+
+class CountBarrier(Barrier):
+    def __init__(self, count):
+        super().__init__()
+        self.count = count
+        self.arrived = 0
+
+    def arrive(self):
+        self.arrived += 1
+        if self.arrived == self.count:
+            self.arrived = 0
+            self.complete()
+
+
+def run_response_ring(slots, consumers, pending, seed, first=0):
+    rng = random.Random(seed)
+    full = [Barrier() for _ in range(slots)]
+    empty = [CountBarrier(consumers) for _ in range(slots)]
+    resp = [("unwritten",)] * slots
+    unread = [0] * slots
+    queue = list(range(100, 100 + pending))   # units of CTAs not launched yet
+    fetched = []                              # response of each fetch, in order
+    f_j, f_state, f_done = 0, "wait_empty", False
+    c_j = [0] * consumers
+    c_done = [False] * consumers
+    while not (f_done and all(c_done)):
+        moves = []
+        i = f_j + first
+        s, par = i % slots, (i // slots) & 1
+        if not f_done:
+            if f_state == "wait_empty" and empty[s].passes(par ^ 1):
+                moves.append(("f_issue",))
+            elif f_state == "in_flight":
+                moves.append(("f_land",))
+            elif f_state == "wait_full" and full[s].passes(par):
+                moves.append(("f_read",))
+        for c in range(consumers):
+            if not c_done[c]:
+                i = c_j[c] + first
+                if full[i % slots].passes((i // slots) & 1):
+                    moves.append(("c", c))
+        if not moves:
+            return f"deadlock: fetcher at {f_j} ({f_state}), readers at {c_j}"
+        mv = rng.choice(moves)
+        if mv[0] == "f_issue":
+            if unread[s]:
+                return f"slot {s} reissued while {unread[s]} readers still owe a read"
+            f_state = "in_flight"
+        elif mv[0] == "f_land":
+            r = queue.pop(0) if queue else None
+            resp[s] = (f_j, r)
+            fetched.append(r)
+            unread[s] = consumers
+            full[s].complete()
+            f_state = "wait_full"
+        elif mv[0] == "f_read":
+            if resp[s] != (f_j, fetched[f_j] if f_j < len(fetched) else "?"):
+                return f"fetcher read {resp[s]} for fetch {f_j}"
+            if resp[s][1] is None:
+                f_done = True
+            else:
+                f_j, f_state = f_j + 1, "wait_empty"
+        else:
+            c = mv[1]
+            i = c_j[c] + first
+            sl = i % slots
+            if resp[sl][0] != c_j[c]:
+                return f"reader {c} took {resp[sl]} for fetch {c_j[c]}"
+            unread[sl] -= 1
+            empty[sl].arrive()
+            if resp[sl][1] is None:
+                c_done[c] = True
+            c_j[c] += 1
+    if fetched[:-1] != list(range(100, 100 + pending)) or fetched[-1] is not None:
+        return f"fetched {fetched}"
+    return None
+
+
+@pytest.mark.parametrize("slots", [1, 2, 3])
+@pytest.mark.parametrize("pending", [0, 1, 2, 3, 7])
+def test_response_ring_holds(slots, pending):
+    for seed in range(60):
+        assert run_response_ring(slots, 6, pending, seed) is None
+
+
+def test_response_ring_numbered_from_one_is_caught():
+    # fetches numbered from 1: the first use of slot 0 waits on parity 1 and passes at
+    # once on a fresh barrier, so a reader takes a response that was never written
+    failures = [run_response_ring(2, 6, 3, seed, first=1) for seed in range(40)]
+    assert all(f is not None for f in failures)

@@ -107,3 +107,75 @@ def test_watchdog_fires_and_context_survives(variant):
     torch.cuda.synchronize()
     assert tg.tg_device_status() == 0
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "after watchdog")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (2560, 2560, 256), (4096, 4096, 192),
+                                   (8192, 8192, 128), (4000, 7000, 128)])
+def test_dynamic_persistence_runs_every_unit_once(M, N, K):
+    # cluster launch control: one CTA per unit; a running CTA takes over the units of CTAs
+    # not launched yet.  Which CTA runs which unit is up to the hardware; what is fixed is
+    # the set of units and the decode of each (the oracle's, with the tail split of a
+    # launch over all SMs), and that a CTA starts with the unit of its own index.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shape = tg.tg_gemm_launch_shape(M, N, K, "single", dynamic=True)
+    units = shape["units"]
+    assert shape["ctas"] == units
+    want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], sms,
+                                    tg.tg_gemm_config()["group"], split_tail=True)
+    assert len(want) == units
+    decode = {worker + w * sms: (bx, by, part) for (worker, w, bx, by, part) in want}
+    a, b = wl.small_int_inputs(M, N, K, "bf16", seed=K)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
+    assert tg.tg_gemm_persistent_debug(a.cuda(), b.cuda(), c, M, N, K, "bf16", variant="single",
+                                       trace=trace, dynamic=True,
+                                       watchdog_ns=1_000_000_000) == 0
+    got = trace.cpu().numpy()
+    per_cta = {}
+    for u in range(units):
+        cta, w, bx, by, part = (int(v) for v in got[u])
+        assert (bx, by, part) == decode[u], u
+        assert 0 <= cta < units
+        if w == 0:
+            assert cta == u, (u, cta)
+        per_cta.setdefault(cta, []).append(w)
+    for cta, ws in per_cta.items():
+        assert sorted(ws) == list(range(len(ws))), cta
+    assert sum(len(ws) for ws in per_cta.values()) == units
+    # integer inputs: every partial sum is exact, so the product is bit-exact
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
+
+
+def test_dynamic_persistence_matches_oracle_on_uniform_inputs():
+    M, N, K = 4000, 7000, 2048
+    a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=5)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tg.tg_gemm_persistent_ex(a.cuda(), b.cuda(), c, M, N, K, "bf16", variant="single",
+                             dynamic=True)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "dynamic")
+
+
+def test_dynamic_persistence_watchdog():
+    M, N, K = 512, 512, 1024
+    a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=1)
+    a_d, b_d = a.cuda(), b.cuda()
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant="single", dynamic=True,
+                                    watchdog_ns=20_000_000, inject_skip_phase=5)
+    assert e.value.code == tg.TG_ERR_TIMEOUT
+    assert tg.tg_device_status() == 0
+    tg.tg_gemm_persistent_ex(a_d, b_d, c, M, N, K, "bf16", variant="single", dynamic=True)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "after watchdog")
+
+
+def test_dynamic_needs_single_variant():
+    a = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty_like(a)
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent_ex(a, a, c, 256, 256, 256, "bf16", variant="pair", dynamic=True)
+    assert e.value.code == tg.TG_ERR_ARG
