@@ -2,7 +2,7 @@
 """Throughput of the persistent warp-specialized GEMM on GB300: one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tg|reference]
-                    [--workload gemm_8192_bf16]
+                    [--workload gemm_8192_bf16 | mxfp8_8192]
 
 A step is one pass of the whole hot path: one tg_gemm_persistent call (one kernel launch)
 on the workload's seeded synthetic inputs, already resident in HBM.  ``value`` is
@@ -286,6 +286,38 @@ def workload_config(w):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def timed_region(step, steps, warm, dev, stream, world):
+    """W untimed steps, then K steps between CUDA events on ``stream`` with a barrier and a
+    device synchronisation on both sides and nvidia-smi clocks sampled meanwhile.  Returns
+    (this rank's ms per step, max over ranks, clocks)."""
+    import torch
+
+    import persistent_warp_specialized_gb300 as tg
+
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize(dev)
+    tg.tg_device_status(stream)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    ms_local = ev0.elapsed_time(ev1) / steps
+    tg.tg_device_status(stream)
+    return ms_local, max_over_ranks(ms_local, dev if world > 1 else None), clocks
+
+
 def run_tg(args):
     import torch
 
@@ -319,30 +351,10 @@ def run_tg(args):
             tg.tg_gemm_persistent_ex(a, b, c, w.M, w.N, w.K, w.dtype, stream, args.variant)
 
     steps, warm = max(1, args.steps), max(3, args.warmup)
-    for _ in range(warm):
-        step()
-    torch.cuda.synchronize(dev)
-    tg.tg_device_status(stream)
-
-    sampler = ClockSampler(dev.index)
-    sampler.start()
-    barrier()
-    torch.cuda.synchronize(dev)
+    ms_local, ms, clocks = timed_region(step, steps, warm, dev, stream, world)
+    value = world * w.flops / (ms * 1e-3) / 1e12
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    t0 = time.time()
-    ev0.record(stream)
-    for _ in range(steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    barrier()
-    clocks = sampler.stop(t0, t1)
-    ms_local = ev0.elapsed_time(ev1) / steps
-    tg.tg_device_status(stream)
-    ms = max_over_ranks(ms_local, dev if world > 1 else None)
-    value = world * w.flops / (ms * 1e-3) / 1e12
 
     # end to end through the host-buffer entry point: H2D A, B + kernel + D2H C per step
     a_h, b_h = a_cpu.pin_memory(), b_cpu.pin_memory()
@@ -429,8 +441,177 @@ def run_tg(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- MXFP8 workload
+MX_METRIC = "block-scaled MXFP8 GEMM TFLOP/s (2MNK/t) at 8192³ on 1 GB300; % of dense fp8 tensor peak"
+
+
+def mx_oracle_slab(a, sa, b, sb, rows):
+    from oracle import mx
+
+    return mx.gemm_mxfp8_ref(a[:rows], sa[:rows], b, sb, "bf16")
+
+
+def mx_config(M, N, K, seed):
+    return {"workload": "mxfp8_8192", "M": M, "N": N, "K": K, "in_dtype": "e4m3",
+            "scale": "e8m0 per 32 K-elements of each A row and B column", "out_dtype": "bf16",
+            "accumulate": "fp32", "inputs": f"MX-quantized N(0,1) / N(0,1/K) draws, seed {seed}",
+            "l2": "inputs larger than L2 (no flush)",
+            "tile": "128 x 256 x 128 bytes, 4 stages; persistent: one CTA per SM"}
+
+
+def run_reference_mx(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    M, N, K, seed = wl.MX_WORKLOADS[args.workload]
+    a, sa, b, sb = (t.numpy() for t in wl.make_mx_inputs(M, N, K, seed))
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    per_step = max(0.05, min(2.0, 150.0 / (steps + warm)))
+    probe = 16
+    t0 = time.perf_counter()
+    mx_oracle_slab(a, sa, b, sb, probe)
+    rows = int(max(min(M, probe * per_step / max(time.perf_counter() - t0, 1e-6)), 8))
+    for _ in range(warm):
+        mx_oracle_slab(a, sa, b, sb, rows)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        mx_oracle_slab(a, sa, b, sb, rows)
+    dt = time.perf_counter() - t0
+    value = 2.0 * rows * N * K * steps / dt / 1e12
+    sample = (f"rows [0, {rows}) of the MXFP8 product ({rows} x {N} outputs, K={K}) per step: "
+              f"decode, scale, binary64 product, round to bf16")
+    print(json.dumps({
+        "impl": "reference", "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": mx_config(M, N, K, seed),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def run_tg_mx(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist(world, "nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import persistent_warp_specialized_gb300 as tg
+    from persistent_warp_specialized_gb300 import _build
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    _build.build()
+    tg.load_library()
+    M, N, K, seed = wl.MX_WORKLOADS[args.workload]
+    host = wl.make_mx_inputs(M, N, K, seed)
+    a, sa, b, sb = (t.to(dev) for t in host)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flops = 2.0 * M * N * K
+
+    def step():
+        tg.tg_gemm_mxfp8(a, sa, b, sb, c, M, N, K, "bf16", stream)
+
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+    ms_local, ms, clocks = timed_region(step, steps, warm, dev, stream, world)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs copied in, the GEMM, C copied out, one stream
+    pinned = [t.pin_memory() for t in host]
+    dev2 = [torch.empty_like(t, device=dev) for t in host]
+    c2 = torch.empty_like(c)
+    c_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for d, h in zip(dev2, pinned):
+            d.copy_(h, non_blocking=True)
+        tg.tg_gemm_mxfp8(*dev2, c2, M, N, K, "bf16", stream)
+        c_h.copy_(c2, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, args.e2e_steps)
+    barrier()
+    ev0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e_steps, dev if world > 1 else None)
+    tg.tg_device_status(stream)
+    e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": sum(t.numel() for t in host), "d2h_bytes_per_step": 2 * M * N,
+           "ms_per_step": e_ms}
+
+    peaks, peak_src = measured_peaks()
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "kernel": "gemm_mxfp8_ws",
+                "traffic": profile_traffic("gemm_mxfp8_ws", "8192_mxfp8"),
+                "peak_source": f"{peak_src}: bf16 burst peak x 2 (the nominal dense fp8 / bf16 "
+                               f"ratio, 4.5 / 2.25 PFLOP/s)",
+                "frac_of_nominal_dense": achieved / (2 * NOMINAL_DENSE_BF16_TFLOPS),
+                "nominal_dense_tflops": 2 * NOMINAL_DENSE_BF16_TFLOPS}
+    line = {
+        "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; see config.inputs)",
+        "config": dict(mx_config(M, N, K, seed), sms=sms),
+        "gpu_launches": steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+
+        from oracle import formats
+
+        an, san, bn, sbn = (t.numpy() for t in host)
+        probe = 16
+        t_0 = time.perf_counter()
+        mx_oracle_slab(an, san, bn, sbn, probe)
+        rows = int(max(min(M, probe * args.cpu_seconds / max(time.perf_counter() - t_0, 1e-6)), 8))
+        t_0 = time.perf_counter()
+        ref = mx_oracle_slab(an, san, bn, sbn, rows)
+        dt = time.perf_counter() - t_0
+        got = formats.decode(wl.bits(c[:rows].cpu()), "bf16")
+        want = formats.decode(ref, "bf16")
+        err = np.abs(got - want)
+        ok = bool(np.isfinite(got).all() and (err <= 5e-3 + 1e-2 * np.abs(want)).all())
+        line["cpu_baseline"] = {
+            "value": 2.0 * rows * N * K / dt / 1e12, "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"rows [0, {rows}) of C ({rows} x {N} outputs, K={K}): decode, scale, "
+                      f"binary64 product (numpy/OpenBLAS), round to bf16; {dt:.1f} s"}
+        line["parity_sample"] = {"rows": rows, "cols": N, "within_tolerance": ok,
+                                 "max_abs_err": float(err.max())}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    if args.workload in wl.MX_WORKLOADS:
+        return run_reference_mx(args) if args.impl == "reference" else run_tg_mx(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_tg(args)

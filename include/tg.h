@@ -181,6 +181,40 @@ int tg_gemm_persistent_host(const void* A_host, const void* B_host, void* C_host
                             void* A_dev, void* B_dev, void* C_dev,
                             int64_t M, int64_t N, int64_t K, int dtype, void* stream);
 
+/*
+ * tg_gemm_mxfp8 -- block-scaled MXFP8 GEMM on ``stream``:
+ *
+ *   C[i, j] = sum_k A[i, k] * 2^(SFA[i, k / 32] - 127) * B[j, k] * 2^(SFB[j, k / 32] - 127)
+ *
+ * The second workload of "[Feature] Introduce tile scheduler #2441"
+ * (examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py), on the same persistent
+ * scheduler and warp roles; the formats are the OCP Microscaling ones ("1d1d": A scaled per
+ * row and B per column, along K only, one scale per 32 elements).
+ *   A_dev [M, K] and B_dev [N, K]: E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3
+ *     fraction bits), row-major -- both K-contiguous, so B is passed as N rows of K.
+ *   SFA_dev [M, K / 32] and SFB_dev [N, K / 32]: E8M0 bytes (2^(e - 127)), row-major.
+ *   C_dev [M, N]: out_dtype (TG_BF16 or TG_F16), row-major; products are accumulated in fp32
+ *     and rounded once to nearest even.
+ *   M, N, K >= 0 and < 2^31; K % 128 == 0; N % 8 == 0.  A, B and C 16-byte aligned, SFA and
+ *   SFB 4-byte aligned.  C must not overlap any input.  M == 0 or N == 0: nothing is done.
+ *   K == 0: C is zero-filled.
+ * The launch is that of TG_VARIANT_SINGLE (tg_gemm_launch_shape): one persistent CTA per SM,
+ * 128 x 256 output tiles, grouped order with the tail split.  Asynchronous; errors as for
+ * tg_gemm_persistent.  Inputs that hold NaN patterns give unspecified outputs.
+ */
+int tg_gemm_mxfp8(const void* A_dev, const void* SFA_dev, const void* B_dev, const void* SFB_dev,
+                  void* C_dev, int64_t M, int64_t N, int64_t K, int out_dtype, void* stream);
+
+/*
+ * tg_gemm_mxfp8_debug -- tg_gemm_mxfp8, synchronously, with the inspection aids of
+ * tg_gemm_persistent_debug (trace of 5 int32 per unit, watchdog limit, injected missing fill).
+ *   flags: 0, or TG_SCHEDULE_PLAIN and/or TG_SCHEDULE_COLUMN_MAJOR (others: TG_ERR_ARG).
+ */
+int tg_gemm_mxfp8_debug(const void* A_dev, const void* SFA_dev, const void* B_dev,
+                        const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,
+                        int out_dtype, void* stream, int flags, int32_t* trace_dev,
+                        uint64_t watchdog_ns, int64_t inject_skip_phase);
+
 #ifdef __cplusplus
 }
 #endif

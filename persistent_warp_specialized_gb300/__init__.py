@@ -44,6 +44,8 @@ EXPORTED = (
     "tg_gemm_persistent_debug",
     "tg_device_status",
     "tg_gemm_persistent_host",
+    "tg_gemm_mxfp8",
+    "tg_gemm_mxfp8_debug",
 )
 
 
@@ -88,6 +90,11 @@ def load_library(path=LIB_PATH):
     lib.tg_device_status.restype = i32
     lib.tg_gemm_persistent_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.tg_gemm_persistent_host.restype = i32
+    lib.tg_gemm_mxfp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.tg_gemm_mxfp8.restype = i32
+    lib.tg_gemm_mxfp8_debug.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
+                                        i64]
+    lib.tg_gemm_mxfp8_debug.restype = i32
     _lib = lib
     return lib
 
@@ -205,6 +212,26 @@ def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True, col
         TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
     n = _check(load_library().tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, flags, buf))
     return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
+
+
+def _mx_flags(plain=False, column_major=False):
+    return (TG_SCHEDULE_PLAIN if plain else 0) | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
+
+
+def tg_gemm_mxfp8(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None):
+    """Block-scaled MXFP8 GEMM: A [M, K], B [N, K] E4M3 bytes; SFA [M, K/32], SFB [N, K/32]
+    E8M0 bytes; C [M, N] in ``out_dtype``."""
+    return _check(load_library().tg_gemm_mxfp8(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
+        _stream(stream)))
+
+
+def tg_gemm_mxfp8_debug(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None, trace=None,
+                        watchdog_ns=0, inject_skip_phase=-1, plain=False, column_major=False):
+    return _check(load_library().tg_gemm_mxfp8_debug(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
+        _stream(stream), _mx_flags(plain, column_major), _ptr(trace), watchdog_ns,
+        inject_skip_phase))
 
 
 def gemm(a, b, out=None, stream=None):

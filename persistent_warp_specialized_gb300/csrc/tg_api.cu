@@ -115,22 +115,31 @@ bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
   return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
-int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer, const char* name) {
+// A row-major [outer, inner] matrix of ``elem_bytes``-byte elements, boxes of
+// box_outer rows x box_inner elements landing with the 128-byte swizzle.
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t elem_bytes, const void* base,
+                 uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                 const char* name) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * tg::kElemBytes};  // bytes between rows
+  const cuuint64_t strides[1] = {inner * elem_bytes};  // bytes between rows
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
   return TG_OK;
+}
+
+int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer, const char* name) {
+  return encode_tiled(map,
+                      dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      tg::kElemBytes, base, inner, outer, box_inner, box_outer, name);
 }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
@@ -274,9 +283,126 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   return TG_OK;
 }
 
+// ---------------------------------------------------------------- block-scaled MXFP8
+int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
+                int64_t M, int64_t N, int64_t K, int out_dtype, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (out_dtype != TG_F16 && out_dtype != TG_BF16)
+    return fail(TG_ERR_ARG, "unknown output dtype %d", out_dtype);
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(TG_ERR_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                (long long)N, (long long)K);
+  if (M == 0 || N == 0) {
+    *nothing_to_do = true;
+    return TG_OK;
+  }
+  if (!C || (K > 0 && (!A || !B || !SFA || !SFB))) return fail(TG_ERR_ARG, "null matrix pointer");
+  if (K % tg::kMxBK != 0)
+    return fail(TG_ERR_ALIGN, "K=%lld must be a multiple of %d (whole scale words per row)",
+                (long long)K, tg::kMxBK);
+  if (N % 8 != 0) return fail(TG_ERR_ALIGN, "N=%lld must be a multiple of 8", (long long)N);
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) ||
+      (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u))))
+    return fail(TG_ERR_ALIGN, "A, B and C must be 16-byte aligned");
+  if (K > 0 && ((reinterpret_cast<uintptr_t>(SFA) & 3u) || (reinterpret_cast<uintptr_t>(SFB) & 3u)))
+    return fail(TG_ERR_ALIGN, "SFA and SFB must be 4-byte aligned");
+  const uint64_t m_blocks = (M + tg::kBM - 1) / tg::kBM, n_blocks = (N + tg::kBN - 1) / tg::kBN;
+  if (m_blocks * n_blocks > static_cast<uint64_t>(kMaxDim))
+    return fail(TG_ERR_ARG, "too many output tiles");
+  int rc;
+  if ((rc = check_device_ptr(C, "C")) != TG_OK) return rc;
+  if (K > 0) {
+    if ((rc = check_device_ptr(A, "A")) != TG_OK) return rc;
+    if ((rc = check_device_ptr(B, "B")) != TG_OK) return rc;
+    if ((rc = check_device_ptr(SFA, "SFA")) != TG_OK) return rc;
+    if ((rc = check_device_ptr(SFB, "SFB")) != TG_OK) return rc;
+    const uint64_t cb = uint64_t(M) * N * tg::kElemBytes;
+    const uint64_t sfk = uint64_t(K) / tg::kMxBlock;
+    if (overlaps(C, cb, A, uint64_t(M) * K) || overlaps(C, cb, B, uint64_t(N) * K) ||
+        overlaps(C, cb, SFA, uint64_t(M) * sfk) || overlaps(C, cb, SFB, uint64_t(N) * sfk))
+      return fail(TG_ERR_ARG, "C overlaps an input");
+  }
+  return TG_OK;
+}
+
+int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M,
+            int64_t N, int64_t K, int out_dtype, void* stream, int flags, bool debug,
+            int32_t* trace, uint64_t watchdog_ns, int64_t inject) {
+  if (flags & ~(TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR))
+    return fail(TG_ERR_ARG, "unknown MXFP8 schedule flags 0x%x", flags);
+  bool nothing = false;
+  int rc = validate_mx(A, SFA, B, SFB, C, M, N, K, out_dtype, &nothing);
+  if (rc != TG_OK || nothing) return rc;
+  int sms = 0, max_pairs = 0;
+  if ((rc = device_ready(&sms, &max_pairs)) != TG_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = tg::launch_zero_fill(C, uint64_t(M) * N * tg::kElemBytes, s);
+    return e == cudaSuccess ? TG_OK : fail_cuda("zero fill launch", e);
+  }
+  tg::MxLaunch l;
+  if ((rc = encode_tiled(&l.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, tg::kMxBK, tg::kBM,
+                         "A")) != TG_OK)
+    return rc;
+  if ((rc = encode_tiled(&l.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, tg::kMxBK,
+                         tg::kBN / 2, "B")) != TG_OK)
+    return rc;
+  if ((rc = encode_2d(&l.tmC, out_dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
+  const Shape sh = launch_shape(M, N, K, TG_VARIANT_SINGLE, (flags & TG_SCHEDULE_PLAIN) != 0,
+                                false, sms, max_pairs);
+  l.SFA = SFA;
+  l.SFB = SFB;
+  l.M = static_cast<uint32_t>(M);
+  l.N = static_cast<uint32_t>(N);
+  l.K = static_cast<uint32_t>(K);
+  l.m_blocks = sh.m_tiles;
+  l.n_blocks = sh.n_tiles;
+  l.k_blocks = static_cast<uint32_t>(K / tg::kMxBK);
+  l.group = tg::kGroup;
+  l.split_from = sh.split_from;
+  l.total_units = sh.units;
+  l.column_major = (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
+  l.grid = sh.ctas;
+  l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
+  l.trace = trace;
+  l.inject_skip_phase = inject;
+  cudaError_t e;
+  if (debug && (e = tg::clear_watchdog_status(s)) != cudaSuccess)
+    return fail_cuda("clearing the watchdog word", e);
+  if ((e = tg::launch_mxfp8(out_dtype, debug, l, s)) != cudaSuccess)
+    return fail_cuda("MXFP8 GEMM launch", e);
+  if (debug) {
+    unsigned int st = 0;
+    if ((e = tg::read_and_clear_watchdog_status(&st, s)) != cudaSuccess)
+      return fail_cuda("MXFP8 GEMM execution", e);
+    if (st)
+      return fail(TG_ERR_TIMEOUT, "watchdog: a wait gave up (roles 0x%x: 1 producer, 2 MMA, "
+                  "4 epilogue, 8 shutdown)", st);
+  }
+  return TG_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int tg_gemm_mxfp8(const void* A_dev, const void* SFA_dev, const void* B_dev, const void* SFB_dev,
+                  void* C_dev, int64_t M, int64_t N, int64_t K, int out_dtype, void* stream) {
+  return mx_impl(A_dev, SFA_dev, B_dev, SFB_dev, C_dev, M, N, K, out_dtype, stream, 0, false,
+                 nullptr, 0, -1);
+}
+
+int tg_gemm_mxfp8_debug(const void* A_dev, const void* SFA_dev, const void* B_dev,
+                        const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,
+                        int out_dtype, void* stream, int flags, int32_t* trace_dev,
+                        uint64_t watchdog_ns, int64_t inject_skip_phase) {
+  if (trace_dev) {
+    int rc = check_device_ptr(trace_dev, "trace");
+    if (rc != TG_OK) return rc;
+  }
+  return mx_impl(A_dev, SFA_dev, B_dev, SFB_dev, C_dev, M, N, K, out_dtype, stream, flags, true,
+                 trace_dev, watchdog_ns, inject_skip_phase);
+}
 
 int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev, int64_t M, int64_t N,
                        int64_t K, int dtype, void* stream) {

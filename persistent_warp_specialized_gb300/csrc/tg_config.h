@@ -113,6 +113,44 @@ static_assert(kPairSmemBytes + 256 <= 232448, "shared memory per CTA (pair varia
 static_assert(kPairBNHalf % kBChunkCols == 0, "pair B half must be whole 64-column chunks");
 static_assert(kPairBK % kKAtom == 0 && kPairBK <= 256, "pair block_K: a multiple of 64, <= 256");
 
+// Block-scaled MXFP8 kernel (the PR's gemm_mxfp8_blockscaled_1d1d): E4M3 A [M, K] and B [N, K],
+// both K-major, one E8M0 scale per 32 K-elements of each A row and each B column, fp32
+// accumulation, bf16/fp16 out; one CTA per 128 x 256 output tile on the same scheduler.
+//   block_K = 128 one-byte elements: one 128-byte swizzle row, four MMAs of K = 32, and the
+//   4 scales of each row that one 32-bit TMEM word holds.
+//   Scales: per stage, 128 A rows and 256 B columns x 4 bytes, gathered by the producer warp
+//   with 4-byte cp.async into 512-byte atoms (row r of an atom at byte (r % 32) * 16 +
+//   (r / 32) * 4), then copied into TMEM by tcgen05.cp .32x128b.warpx4, which replicates
+//   each atom into all four 32-lane quadrants (measured on GB300: the MMA reads the scale
+//   of A row r at lane r, column r / 32, and the scale of B column n at column n / 32 in the
+//   quadrant of the output row it serves).
+//   TMEM: one 256-column accumulator plus 16 scale columns per stage (SFA 4, SFB 8): two
+//   accumulators would take all 512 columns.  The epilogue copies the whole accumulator to
+//   registers before releasing it, so the MMA role waits only for that copy.
+#ifndef TG_MX_STAGES
+#define TG_MX_STAGES 4
+#endif
+constexpr int kMxStages = TG_MX_STAGES;
+constexpr int kMxBK = 128;                                     // K elements (bytes) per stage
+constexpr int kMxBlock = 32;                                   // elements per scale
+constexpr int kMxUmmaK = 32;                                   // K of one kind::mxf8f6f4 MMA
+constexpr uint32_t kMxABytes = kBM * kMxBK;                    // 16 KiB
+constexpr uint32_t kMxBHalfBytes = (kBN / 2) * kMxBK;          // 16 KiB: 128 columns of B
+constexpr uint32_t kMxBBytes = kBN * kMxBK;                    // 32 KiB
+constexpr uint32_t kMxStageBytes = kMxABytes + kMxBBytes;      // 48 KiB
+constexpr uint32_t kMxSfAtomBytes = 512;                       // 128 rows x 4 scales
+constexpr uint32_t kMxSfStageBytes = 3 * kMxSfAtomBytes;       // SFA atom + two SFB atoms
+constexpr uint32_t kMxSfRegionBytes = (kMxStages * kMxSfStageBytes + 1023u) & ~1023u;
+constexpr uint32_t kMxEpiSmemBytes = kEpiWarps * kEpiBufBytes; // one staging buffer per warp
+constexpr uint32_t kMxSmemBytes =
+    kSmemAlignSlack + kMxStages * kMxStageBytes + kMxSfRegionBytes + kMxEpiSmemBytes;
+constexpr uint32_t kMxAccCols = kBN;                           // TMEM columns [0, 256)
+constexpr uint32_t kMxSfColsPerStage = 16;
+constexpr uint32_t kMxLoadedArrivals = 1 + 32;                 // expect_tx + one per producer lane
+static_assert(kMxSmemBytes + 256 <= 232448, "shared memory per CTA (MXFP8)");
+static_assert(kMxAccCols + kMxStages * kMxSfColsPerStage <= kTmemCols, "MXFP8 TMEM budget");
+static_assert(kMxBK % (4 * kMxBlock) == 0 && kMxBK == 128, "one scale word per row and stage");
+
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;
 constexpr uint32_t kRoleMma = 2u;

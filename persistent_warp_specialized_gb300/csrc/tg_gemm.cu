@@ -1,9 +1,11 @@
 // tg_gemm.cu -- instantiations and launchers of the sm_103a kernels behind the C ABI:
 // the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
-// tile-schedule inspection kernel, and the zero fill used when K == 0.
+// block-scaled MXFP8 GEMM, the tile-schedule inspection kernel, and the zero fill used when
+// K == 0.  All kernels share this translation unit's watchdog status word.
 #include "tg_gemm_kernel.cuh"
 #include "tg_gemm_pair_kernel.cuh"
 #include "tg_internal.h"
+#include "tg_mx_kernel.cuh"
 
 namespace tg {
 
@@ -87,6 +89,37 @@ cudaError_t set_smem_attr() {
                               static_cast<int>(kPairSmemBytes));
 }
 
+template <int OUT, bool DEBUG>
+cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
+  MxParams p;
+  p.SFA = static_cast<const uint8_t*>(l.SFA);
+  p.SFB = static_cast<const uint8_t*>(l.SFB);
+  p.M = l.M;
+  p.N = l.N;
+  p.K = l.K;
+  p.sf_row_bytes = l.K / kMxBlock;
+  p.m_blocks = l.m_blocks;
+  p.n_blocks = l.n_blocks;
+  p.k_blocks = l.k_blocks;
+  p.group = l.group;
+  p.split_from = l.split_from;
+  p.total_units = l.total_units;
+  p.column_major = l.column_major;
+  p.watchdog_ns = l.watchdog_ns;
+  p.trace = l.trace;
+  p.inject_skip_phase = l.inject_skip_phase;
+  gemm_mxfp8_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxSmemBytes, stream>>>(l.tmA, l.tmB,
+                                                                                l.tmC, p);
+  return cudaGetLastError();
+}
+
+template <int OUT, bool DEBUG>
+cudaError_t set_mx_smem_attr() {
+  return cudaFuncSetAttribute(gemm_mxfp8_ws_kernel<OUT, DEBUG>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kMxSmemBytes));
+}
+
 }  // namespace
 
 cudaError_t prepare_gemm_kernels(int* max_pairs) {
@@ -95,6 +128,10 @@ cudaError_t prepare_gemm_kernels(int* max_pairs) {
   if ((e = set_smem_attr<1, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<0, true>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<1, true>()) != cudaSuccess) return e;
+  if ((e = set_mx_smem_attr<0, false>()) != cudaSuccess) return e;
+  if ((e = set_mx_smem_attr<1, false>()) != cudaSuccess) return e;
+  if ((e = set_mx_smem_attr<0, true>()) != cudaSuccess) return e;
+  if ((e = set_mx_smem_attr<1, true>()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -122,6 +159,11 @@ cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
   }
   if (dtype == 0) return debug ? launch_one<0, true>(l, stream) : launch_one<0, false>(l, stream);
   return debug ? launch_one<1, true>(l, stream) : launch_one<1, false>(l, stream);
+}
+
+cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream) {
+  if (out_dtype == 0) return debug ? launch_mx<0, true>(l, stream) : launch_mx<0, false>(l, stream);
+  return debug ? launch_mx<1, true>(l, stream) : launch_mx<1, false>(l, stream);
 }
 
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {

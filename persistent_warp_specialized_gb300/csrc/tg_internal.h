@@ -23,6 +23,21 @@ struct GemmLaunch {
   int64_t inject_skip_phase;
 };
 
+// the block-scaled MXFP8 GEMM (one CTA per 128 x 256 tile, the single variant's schedule)
+struct MxLaunch {
+  CUtensorMap tmA, tmB, tmC;
+  const void* SFA;
+  const void* SFB;
+  uint32_t M, N, K;
+  uint32_t m_blocks, n_blocks, k_blocks, group;
+  uint32_t split_from, total_units;
+  uint32_t column_major;
+  uint32_t grid;
+  uint64_t watchdog_ns;
+  int32_t* trace;
+  int64_t inject_skip_phase;
+};
+
 // kernel variants: one CTA per 128 x 256 tile, or a CTA pair (cta_group::2) per 256 x 256 tile
 enum Variant { kVariantSingle = 1, kVariantPair = 2 };
 
@@ -33,6 +48,8 @@ cudaError_t prepare_gemm_kernels(int* max_pairs);
 // counts 256-row pair tiles.
 cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
                         cudaStream_t stream);
+// out_dtype 0 = fp16, 1 = bf16
+cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream);
 // C[0 .. bytes) = 0 (bytes a multiple of 16, C 16-byte aligned)
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream);
 // rows of 5 int32 (worker, w, bx, by, part) over the units [0, units); tiles below

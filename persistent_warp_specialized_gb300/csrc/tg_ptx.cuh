@@ -216,6 +216,63 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// As tmem_ld_32x32b_x64, for 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- block-scaled MMA (MXFP8)
+// 4-byte global -> shared copy (cp.async, L1-allocating); ``src_bytes`` 0 writes zeros and
+// reads nothing.  Both addresses 4-byte aligned.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on ``bar`` once every cp.async this thread issued so far has landed; the arrival
+// counts against the barrier's expected count (noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Shared -> TMEM copy of a 32-row x 16-byte matrix into all four 32-lane quadrants: lane
+// 32q + i, column c + j receives bytes 4j .. 4j + 3 of row i (tcgen05.cp .32x128b.warpx4).
+// Issued by one thread; ordered before tcgen05.mma issued later by the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * 2^SFA) . (B * 2^SFB): E4M3 operands from shared memory, E8M0 scales from
+// TMEM (one per 32 K-elements, byte ids in the instruction descriptor).  One thread issues it.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cluster launch control
 // Ask the hardware to cancel the launch of a cluster that has not started yet.  The 16-byte
 // response is written to [resp] (shared, 16-byte aligned) and completes 16 transaction bytes
@@ -357,6 +414,28 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t m, u
                                                  uint32_t a_mn_major, uint32_t b_mn_major) {
   return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (a_mn_major << 15) |
          (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor without swizzle: core matrices of 8 rows x 16 bytes stored
+// contiguously; ``sbo_bytes`` between consecutive 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with block scaling (32 bit):
+//   [4,6) B scale byte id   [7,10) A type   [10,13) B type   (0 = E4M3)
+//   [15] / [16] A / B major (0 = K-major)   [17,23) N >> 3   [23] scale type (1 = E8M0)
+//   [24,29) M >> 4   [29,31) A scale byte id
+// The byte ids pick which byte of each 32-bit TMEM scale word the instruction reads.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t m, uint32_t n, uint32_t a_sf_id,
+                                                  uint32_t b_sf_id) {
+  return (b_sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (a_sf_id << 29);
 }
 
 }  // namespace tg

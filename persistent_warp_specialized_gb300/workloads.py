@@ -83,3 +83,55 @@ def bits(t):
     import numpy as np
 
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- block-scaled MXFP8 inputs
+# The MXFP8 workload runs at the size of the dense headline (8192^3, bf16 output); the tests
+# add small, ragged and integer-valued cases.
+MX_WORKLOADS = {
+    "mxfp8_8192": (8192, 8192, 8192, 6),   # M, N, K, seed
+}
+MX_BLOCK = 32
+
+
+def _mx_quantize(x):
+    """x [R, K] float32 -> (E4M3 bytes [R, K], E8M0 bytes [R, K/32]) by the OCP Microscaling
+    recipe: per block of 32 along K, shared exponent floor(log2(max |x|)) - 8 (8 = the largest
+    E4M3 exponent), elements x / 2^e saturated to +-448 and cast by torch (round to nearest
+    even); all-zero blocks take the exponent -127."""
+    R, K = x.shape
+    blocks = x.reshape(R, K // MX_BLOCK, MX_BLOCK)
+    amax = blocks.abs().amax(dim=2)
+    e = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, 1.0))) - 8,
+                    torch.full_like(amax, -127.0)).clamp(-127, 127)
+    scaled = (blocks / torch.exp2(e)[:, :, None]).clamp(-448.0, 448.0)
+    q = scaled.reshape(R, K).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    s = (e + 127).to(torch.uint8).contiguous()
+    return q, s
+
+
+def make_mx_inputs(M, N, K, seed=0):
+    """(A [M, K], SFA [M, K/32], B [N, K], SFB [N, K/32]) as CPU uint8 tensors: A and B are
+    N(0, 1) and N(0, 1/K) draws quantized to MXFP8 (so entries of C are O(1))."""
+    gen = torch.Generator().manual_seed(int(seed))
+    a = torch.randn((M, K), generator=gen, dtype=torch.float32)
+    b = torch.randn((N, K), generator=gen, dtype=torch.float32) * (1.0 / float(K) ** 0.5)
+    qa, sa = _mx_quantize(a)
+    qb, sb = _mx_quantize(b)
+    return qa, sa, qb, sb
+
+
+# E4M3 byte patterns of the integers -4 .. 4
+_E4M3_INT = {-4: 0xC8, -3: 0xC4, -2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
+
+
+def mx_int_inputs(M, N, K, seed=0, scale_lo=126, scale_hi=128):
+    """Integer elements in [-4, 4] with scales 2^(s - 127), s in [scale_lo, scale_hi]: every
+    partial sum of the product is exact in fp32 for K up to 2^13."""
+    gen = torch.Generator().manual_seed(int(seed))
+    lut = torch.tensor([_E4M3_INT[v] for v in range(-4, 5)], dtype=torch.uint8)
+    a = lut[torch.randint(0, 9, (M, K), generator=gen)].contiguous()
+    b = lut[torch.randint(0, 9, (N, K), generator=gen)].contiguous()
+    sa = torch.randint(scale_lo, scale_hi + 1, (M, K // MX_BLOCK), generator=gen).to(torch.uint8)
+    sb = torch.randint(scale_lo, scale_hi + 1, (N, K // MX_BLOCK), generator=gen).to(torch.uint8)
+    return a, sa.contiguous(), b, sb.contiguous()

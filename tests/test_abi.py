@@ -88,3 +88,28 @@ def test_product_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not pat.search(text), f
+
+
+def test_mxfp8_host_side_rejections_need_no_gpu(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    cases = [
+        ((16, 16, 16, 16, 16, 8, 8, 128, 7), tg.TG_ERR_ARG),         # unknown output dtype
+        ((16, 16, 16, 16, 16, 8, 8, -128, "bf16"), tg.TG_ERR_ARG),   # negative size
+        ((16, 16, 16, 16, 16, 8, 8, 96, "bf16"), tg.TG_ERR_ALIGN),   # K % 128 != 0
+        ((16, 16, 16, 16, 16, 8, 12, 128, "bf16"), tg.TG_ERR_ALIGN),  # N % 8 != 0
+        ((16, 16, None, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ARG),  # null B
+        ((16, 16, 16, None, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ARG),  # null SFB
+        ((16, 18, 16, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ALIGN),  # SFA not 4-byte aligned
+        ((24, 16, 16, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ALIGN),  # A not 16-byte aligned
+    ]
+    for args, code in cases:
+        with pytest.raises(tg.TgError) as e:
+            tg.tg_gemm_mxfp8(*args, stream=0)
+        assert e.value.code == code, args
+    rc = tg.load_library().tg_gemm_mxfp8_debug(16, 16, 16, 16, 16, 8, 8, 128, 1, 0, 0x400, None,
+                                               0, -1)    # dynamic is not an MXFP8 option
+    assert rc == tg.TG_ERR_ARG
+    assert tg.tg_gemm_mxfp8(None, None, None, None, None, 0, 8, 128, "bf16", stream=0) == 0
+    assert tg.tg_gemm_mxfp8(None, None, None, None, None, 8, 0, 128, "bf16", stream=0) == 0

@@ -1,0 +1,149 @@
+"""GPU: the block-scaled MXFP8 GEMM against the oracle (oracle.mx).
+
+* integer elements with power-of-two scales: every partial sum is exact in fp32, so the
+  CUDA path must equal the oracle bit for bit -- this is what catches a scale read from the
+  wrong row, column, k-block or pipeline stage;
+* MX-quantized normal draws: the acceptance bound |C - C_ref| <= 5e-3 + 1e-2 |C_ref| and the
+  tighter fp32 accumulation bound 2 ulp(C_ref) + gamma_K (|A| . |B|);
+* the debug trace against the oracle's schedule; the watchdog; empty and K = 0 problems;
+* the full 8192^3 workload on sampled rows and columns.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import persistent_warp_specialized_gb300 as tg
+from persistent_warp_specialized_gb300 import workloads as wl
+from oracle import formats, mx, schedule
+
+from gpu_helpers import ATOL, RTOL, ensure_library, nan_filled
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def run_mx(a, sa, b, sb, out="bf16", debug=False, **kw):
+    M, K = a.shape
+    N = b.shape[0]
+    c = nan_filled(M, N, out)
+    dev = [t.cuda() for t in (a, sa, b, sb)]
+    if debug:
+        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, out, **kw)
+    else:
+        tg.tg_gemm_mxfp8(*dev, c, M, N, K, out)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    return wl.bits(c.cpu())
+
+
+def ref_bits(a, sa, b, sb, out="bf16"):
+    return mx.gemm_mxfp8_ref(a.numpy(), sa.numpy(), b.numpy(), sb.numpy(), out)
+
+
+def check_tolerance(c_bits, r_bits, a, sa, b, sb, out, what, gate=True):
+    """The acceptance gate (unless ``gate`` is False) and the fp32 accumulation bound."""
+    c = formats.decode(c_bits, out)
+    r = formats.decode(r_bits, out)
+    assert np.isfinite(c).all(), f"{what}: non-finite outputs"
+    err = np.abs(c - r)
+    if gate:
+        bad = err > ATOL + RTOL * np.abs(r)
+        assert not bad.any(), f"{what}: {int(bad.sum())} outside the gate, first {np.argwhere(bad)[:4].tolist()}"
+    s = np.abs(mx.scaled(a.numpy(), sa.numpy())) @ np.abs(mx.scaled(b.numpy(), sb.numpy())).T
+    K = a.shape[1]
+    u = 2.0 ** -23
+    bound = 2.0 * formats.ulp(r_bits, out) + K * u / (1 - K * u) * s
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} outside the fp32 accumulation bound"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (512, 768, 512), (1000, 520, 384),
+                                   (4096, 4096, 128), (2560, 2560, 256), (8, 8, 128)])
+def test_integer_inputs_are_bit_exact(M, N, K):
+    a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=M + N + K)
+    assert np.array_equal(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1024, 1024, 1024), (1000, 520, 2048),
+                                   (4000, 7000, 2048)])
+def test_quantized_normal_inputs_within_tolerance(M, N, K, out):
+    a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed=7 * M + K)
+    check_tolerance(run_mx(a, sa, b, sb, out), ref_bits(a, sa, b, sb, out), a, sa, b, sb, out,
+                    f"{M}x{N}x{K} {out}")
+
+
+def test_scales_span_the_e8m0_range():
+    # element blocks scaled from 2^-60 to 2^+60 (all products stay normal in fp32).  Here an
+    # output can be the small residue of block terms 10^7 .. 10^13 times larger that cancel,
+    # and no fp32 accumulation order meets the relative gate there (an in-order fp32 sum of
+    # the exact block terms misses it on 8 of these 65536 outputs), so only the fp32
+    # accumulation bound is asserted.
+    M, N, K = 256, 256, 256
+    a, _, b, _ = wl.mx_int_inputs(M, N, K, seed=3)
+    gen = torch.Generator().manual_seed(11)
+    sa = torch.randint(127 - 30, 127 + 31, (M, K // 32), generator=gen).to(torch.uint8)
+    sb = torch.randint(127 - 30, 127 + 31, (N, K // 32), generator=gen).to(torch.uint8)
+    check_tolerance(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb), a, sa, b, sb, "bf16", "scales",
+                    gate=False)
+
+
+@pytest.mark.parametrize("plain,column_major", [(False, False), (True, False), (False, True)])
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4000, 7000, 128), (256, 256, 256)])
+def test_kernel_followed_the_schedule(M, N, K, plain, column_major):
+    shape = tg.tg_gemm_launch_shape(M, N, K, "single", plain)
+    units = shape["units"]
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
+    a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=5)
+    got_c = run_mx(a, sa, b, sb, debug=True, trace=trace, plain=plain, column_major=column_major)
+    want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"],
+                                    tg.tg_gemm_config()["group"], split_tail=not plain,
+                                    column_major=column_major)
+    assert len(want) == units
+    by_unit = {worker + w * shape["workers"]: (worker, w, bx, by, part)
+               for (worker, w, bx, by, part) in want}
+    got = trace.cpu().numpy()
+    for u in range(units):
+        assert tuple(int(v) for v in got[u]) == by_unit[u], u
+    assert np.array_equal(got_c, ref_bits(a, sa, b, sb))
+
+
+def test_watchdog_fires_and_context_survives():
+    M, N, K = 512, 512, 1024
+    a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=1)
+    dev = [t.cuda() for t in (a, sa, b, sb)]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, "bf16", watchdog_ns=20_000_000,
+                               inject_skip_phase=5)
+    assert e.value.code == tg.TG_ERR_TIMEOUT
+    assert tg.tg_device_status() == 0
+    assert np.array_equal(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb))
+
+
+def test_empty_and_zero_k():
+    c = nan_filled(64, 64, "bf16")
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    assert tg.tg_gemm_mxfp8(z, z, z, z, c, 64, 64, 0, "bf16") == 0
+    torch.cuda.synchronize()
+    assert (c.float() == 0).all()
+    assert tg.tg_gemm_mxfp8(None, None, None, None, None, 0, 64, 128, "bf16") == 0
+
+
+def test_full_size_workload_sampled_entries():
+    M, N, K, seed = wl.MX_WORKLOADS["mxfp8_8192"]
+    a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed)
+    c = run_mx(a, sa, b, sb)
+    rng = np.random.default_rng(0)
+    rows = np.concatenate([[0, M - 1], rng.choice(M, 62, replace=False)])
+    cols = np.concatenate([[0, N - 1], rng.choice(N, 62, replace=False)])
+    want = mx.gemm_mxfp8_ref_entries(a.numpy(), sa.numpy(), b.numpy(), sb.numpy(), rows, cols)
+    got = c[np.ix_(rows, cols)]
+    cv, rv = formats.decode(got, "bf16"), formats.decode(want, "bf16")
+    assert np.isfinite(cv).all()
+    assert (np.abs(cv - rv) <= ATOL + RTOL * np.abs(rv)).all()
