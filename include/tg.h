@@ -182,22 +182,44 @@ int tg_gemm_persistent_host(const void* A_host, const void* B_host, void* C_host
                             int64_t M, int64_t N, int64_t K, int dtype, void* stream);
 
 /*
- * tg_gemm_mxfp8 -- block-scaled MXFP8 GEMM on ``stream``:
- *
- *   C[i, j] = sum_k A[i, k] * 2^(SFA[i, k / 32] - 127) * B[j, k] * 2^(SFB[j, k / 32] - 127)
- *
- * The second workload of "[Feature] Introduce tile scheduler #2441"
+ * Block-scaled MXFP8 GEMM: the second workload of "[Feature] Introduce tile scheduler #2441"
  * (examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py), on the same persistent
- * scheduler and warp roles; the formats are the OCP Microscaling ones ("1d1d": A scaled per
- * row and B per column, along K only, one scale per 32 elements).
- *   A_dev [M, K] and B_dev [N, K]: E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3
- *     fraction bits), row-major -- both K-contiguous, so B is passed as N rows of K.
- *   SFA_dev [M, K / 32] and SFB_dev [N, K / 32]: E8M0 bytes (2^(e - 127)), row-major.
+ * scheduler and warp roles, in the OCP Microscaling formats ("1d1d": A scaled per row and B
+ * per column, along K only, one scale per 32 elements):
+ *
+ *   C[i, j] = sum_k A[i, k] * 2^(SA[i, k / 32] - 127) * B[j, k] * 2^(SB[j, k / 32] - 127)
+ *
+ * A [M, K] and B [N, K] hold E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3 fraction
+ * bits), row-major: both K-contiguous, so B is passed as N rows of K.  SA [M, K / 32] and
+ * SB [N, K / 32] hold E8M0 bytes (2^(e - 127)), row-major.  The GEMM reads the scales
+ * packed by tg_mxfp8_pack_scales, the page's scale-factor transpose done ahead of the GEMM
+ * (weights' scales can be packed once).
+ *
+ * Packed layout of the scales of a [rows, K] operand: for each 128-element k-block k and each
+ * block b of 128 rows (rows padded to a multiple of 256), 512 bytes at offset
+ * (k * row_blocks + b) * 512 holding, for r < 128 and j < 4, scale [128 b + r, 4 k + j] at
+ * byte (r % 32) * 16 + (r / 32) * 4 + j (0 for padding rows); row_blocks = 2 * ceil(rows / 256).
+ */
+
+/* Bytes of the packed scales of a [rows, K] operand (K % 128 == 0), or a negative error. */
+int64_t tg_mxfp8_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * tg_mxfp8_pack_scales -- row-major scales sf_dev [rows, K / 32] (4-byte aligned) into
+ * packed_dev (tg_mxfp8_scale_bytes(rows, K) bytes, 16-byte aligned, not overlapping sf_dev),
+ * on ``stream``.  rows >= 0, K % 128 == 0.  Asynchronous.
+ */
+int tg_mxfp8_pack_scales(const void* sf_dev, void* packed_dev, int64_t rows, int64_t K,
+                         void* stream);
+
+/*
+ * tg_gemm_mxfp8 -- C = the block-scaled product above, on ``stream``.
+ *   A_dev [M, K], B_dev [N, K]: E4M3; SFA_dev, SFB_dev: packed scales of A and of B.
  *   C_dev [M, N]: out_dtype (TG_BF16 or TG_F16), row-major; products are accumulated in fp32
  *     and rounded once to nearest even.
- *   M, N, K >= 0 and < 2^31; K % 128 == 0; N % 8 == 0.  A, B and C 16-byte aligned, SFA and
- *   SFB 4-byte aligned.  C must not overlap any input.  M == 0 or N == 0: nothing is done.
- *   K == 0: C is zero-filled.
+ *   M, N, K >= 0 and < 2^31; K % 128 == 0; N % 8 == 0.  All five pointers 16-byte aligned.
+ *   C must not overlap any input.  M == 0 or N == 0: nothing is done.  K == 0: C is
+ *   zero-filled.
  * The launch is that of TG_VARIANT_SINGLE (tg_gemm_launch_shape): one persistent CTA per SM,
  * 128 x 256 output tiles, grouped order with the tail split.  Asynchronous; errors as for
  * tg_gemm_persistent.  Inputs that hold NaN patterns give unspecified outputs.

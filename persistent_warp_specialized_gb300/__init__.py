@@ -46,6 +46,8 @@ EXPORTED = (
     "tg_gemm_persistent_host",
     "tg_gemm_mxfp8",
     "tg_gemm_mxfp8_debug",
+    "tg_mxfp8_scale_bytes",
+    "tg_mxfp8_pack_scales",
 )
 
 
@@ -95,6 +97,10 @@ def load_library(path=LIB_PATH):
     lib.tg_gemm_mxfp8_debug.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
                                         i64]
     lib.tg_gemm_mxfp8_debug.restype = i32
+    lib.tg_mxfp8_scale_bytes.argtypes = [i64, i64]
+    lib.tg_mxfp8_scale_bytes.restype = i64
+    lib.tg_mxfp8_pack_scales.argtypes = [vp, vp, i64, i64, vp]
+    lib.tg_mxfp8_pack_scales.restype = i32
     _lib = lib
     return lib
 
@@ -218,9 +224,28 @@ def _mx_flags(plain=False, column_major=False):
     return (TG_SCHEDULE_PLAIN if plain else 0) | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
 
 
+def tg_mxfp8_scale_bytes(rows, K):
+    return _check(load_library().tg_mxfp8_scale_bytes(rows, K))
+
+
+def tg_mxfp8_pack_scales(sf, packed, rows, K, stream=None):
+    return _check(load_library().tg_mxfp8_pack_scales(_ptr(sf), _ptr(packed), rows, K,
+                                                      _stream(stream)))
+
+
+def mxfp8_pack(sf, K, stream=None):
+    """torch convenience: packed scales of a CUDA uint8 tensor sf [rows, K/32] (a new tensor)."""
+    import torch
+
+    rows = sf.shape[0]
+    out = torch.empty(tg_mxfp8_scale_bytes(rows, K), dtype=torch.uint8, device=sf.device)
+    tg_mxfp8_pack_scales(sf, out, rows, K, stream)
+    return out
+
+
 def tg_gemm_mxfp8(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None):
-    """Block-scaled MXFP8 GEMM: A [M, K], B [N, K] E4M3 bytes; SFA [M, K/32], SFB [N, K/32]
-    E8M0 bytes; C [M, N] in ``out_dtype``."""
+    """Block-scaled MXFP8 GEMM: A [M, K], B [N, K] E4M3 bytes; SFA, SFB their packed E8M0
+    scales (tg_mxfp8_pack_scales); C [M, N] in ``out_dtype``."""
     return _check(load_library().tg_gemm_mxfp8(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
         _stream(stream)))

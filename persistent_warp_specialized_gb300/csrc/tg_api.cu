@@ -284,6 +284,16 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 }
 
 // ---------------------------------------------------------------- block-scaled MXFP8
+// Row blocks (of 128) of a packed scale array: the rows rounded up to a multiple of 256, so
+// that the two atoms of a 256-row B tile always exist.
+uint64_t mx_row_blocks(int64_t rows) {
+  return (uint64_t(rows) + tg::kMxPackRows - 1) / tg::kMxPackRows * (tg::kMxPackRows / tg::kBM);
+}
+
+uint64_t mx_packed_bytes(int64_t rows, int64_t K) {
+  return uint64_t(K) / tg::kMxBK * mx_row_blocks(rows) * tg::kMxSfAtomBytes;
+}
+
 int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                 int64_t M, int64_t N, int64_t K, int out_dtype, bool* nothing_to_do) {
   *nothing_to_do = false;
@@ -304,8 +314,8 @@ int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, 
   if ((reinterpret_cast<uintptr_t>(C) & 15u) ||
       (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u))))
     return fail(TG_ERR_ALIGN, "A, B and C must be 16-byte aligned");
-  if (K > 0 && ((reinterpret_cast<uintptr_t>(SFA) & 3u) || (reinterpret_cast<uintptr_t>(SFB) & 3u)))
-    return fail(TG_ERR_ALIGN, "SFA and SFB must be 4-byte aligned");
+  if (K > 0 && ((reinterpret_cast<uintptr_t>(SFA) & 15u) || (reinterpret_cast<uintptr_t>(SFB) & 15u)))
+    return fail(TG_ERR_ALIGN, "SFA and SFB must be 16-byte aligned");
   const uint64_t m_blocks = (M + tg::kBM - 1) / tg::kBM, n_blocks = (N + tg::kBN - 1) / tg::kBN;
   if (m_blocks * n_blocks > static_cast<uint64_t>(kMaxDim))
     return fail(TG_ERR_ARG, "too many output tiles");
@@ -317,9 +327,8 @@ int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, 
     if ((rc = check_device_ptr(SFA, "SFA")) != TG_OK) return rc;
     if ((rc = check_device_ptr(SFB, "SFB")) != TG_OK) return rc;
     const uint64_t cb = uint64_t(M) * N * tg::kElemBytes;
-    const uint64_t sfk = uint64_t(K) / tg::kMxBlock;
     if (overlaps(C, cb, A, uint64_t(M) * K) || overlaps(C, cb, B, uint64_t(N) * K) ||
-        overlaps(C, cb, SFA, uint64_t(M) * sfk) || overlaps(C, cb, SFB, uint64_t(N) * sfk))
+        overlaps(C, cb, SFA, mx_packed_bytes(M, K)) || overlaps(C, cb, SFB, mx_packed_bytes(N, K)))
       return fail(TG_ERR_ARG, "C overlaps an input");
   }
   return TG_OK;
@@ -348,6 +357,8 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
                          tg::kBN / 2, "B")) != TG_OK)
     return rc;
   if ((rc = encode_2d(&l.tmC, out_dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
+  l.sfa_blocks = static_cast<uint32_t>(mx_row_blocks(M));
+  l.sfb_blocks = static_cast<uint32_t>(mx_row_blocks(N));
   const Shape sh = launch_shape(M, N, K, TG_VARIANT_SINGLE, (flags & TG_SCHEDULE_PLAIN) != 0,
                                 false, sms, max_pairs);
   l.SFA = SFA;
@@ -385,6 +396,38 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
 }  // namespace
 
 extern "C" {
+
+int64_t tg_mxfp8_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0 || rows > kMaxDim || K > kMaxDim)
+    return fail(TG_ERR_ARG, "sizes must be in [0, 2^31): rows=%lld K=%lld", (long long)rows,
+                (long long)K);
+  if (K % tg::kMxBK != 0)
+    return fail(TG_ERR_ALIGN, "K=%lld must be a multiple of %d", (long long)K, tg::kMxBK);
+  return static_cast<int64_t>(mx_packed_bytes(rows, K));
+}
+
+int tg_mxfp8_pack_scales(const void* sf_dev, void* packed_dev, int64_t rows, int64_t K,
+                         void* stream) {
+  const int64_t bytes = tg_mxfp8_scale_bytes(rows, K);
+  if (bytes < 0) return static_cast<int>(bytes);
+  if (bytes == 0) return TG_OK;
+  if (!packed_dev || (rows > 0 && !sf_dev)) return fail(TG_ERR_ARG, "null scale pointer");
+  if ((reinterpret_cast<uintptr_t>(packed_dev) & 15u) ||
+      (rows > 0 && (reinterpret_cast<uintptr_t>(sf_dev) & 3u)))
+    return fail(TG_ERR_ALIGN, "packed scales must be 16-byte aligned, row-major scales 4-byte");
+  int rc;
+  if ((rc = check_device_ptr(packed_dev, "packed scales")) != TG_OK) return rc;
+  if (rows > 0) {
+    if ((rc = check_device_ptr(sf_dev, "scales")) != TG_OK) return rc;
+    if (overlaps(sf_dev, uint64_t(rows) * K / tg::kMxBlock, packed_dev, uint64_t(bytes)))
+      return fail(TG_ERR_ARG, "packed scales overlap the row-major scales");
+  }
+  cudaError_t e = tg::launch_mx_pack(sf_dev, packed_dev, static_cast<uint32_t>(rows),
+                                     static_cast<uint32_t>(K / tg::kMxBK),
+                                     static_cast<uint32_t>(mx_row_blocks(rows)),
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TG_OK : fail_cuda("scale pack launch", e);
+}
 
 int tg_gemm_mxfp8(const void* A_dev, const void* SFA_dev, const void* B_dev, const void* SFB_dev,
                   void* C_dev, int64_t M, int64_t N, int64_t K, int out_dtype, void* stream) {

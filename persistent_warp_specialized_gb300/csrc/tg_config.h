@@ -118,12 +118,15 @@ static_assert(kPairBK % kKAtom == 0 && kPairBK <= 256, "pair block_K: a multiple
 // accumulation, bf16/fp16 out; one CTA per 128 x 256 output tile on the same scheduler.
 //   block_K = 128 one-byte elements: one 128-byte swizzle row, four MMAs of K = 32, and the
 //   4 scales of each row that one 32-bit TMEM word holds.
-//   Scales: per stage, 128 A rows and 256 B columns x 4 bytes, gathered by the producer warp
-//   with 4-byte cp.async into 512-byte atoms (row r of an atom at byte (r % 32) * 16 +
-//   (r / 32) * 4), then copied into TMEM by tcgen05.cp .32x128b.warpx4, which replicates
-//   each atom into all four 32-lane quadrants (measured on GB300: the MMA reads the scale
-//   of A row r at lane r, column r / 32, and the scale of B column n at column n / 32 in the
-//   quadrant of the output row it serves).
+//   Scales reach the kernel packed (tg_mxfp8_pack_scales): for each 128-element k-block and
+//   each block of 128 rows, one 512-byte atom with row r's 4 scales at byte (r % 32) * 16 +
+//   (r / 32) * 4 -- the source layout of tcgen05.cp .32x128b.warpx4, which replicates an atom
+//   into all four 32-lane TMEM quadrants (measured on GB300: the MMA reads the scale of A row r
+//   at lane r, column r / 32, and that of B column n at column n / 32 in the quadrant of the
+//   output row it serves).  The producer bulk-copies a stage's atoms (512 bytes of A, 1 KiB
+//   of B) with its operands, on the same barrier.  (Reordering row-major scales inside the
+//   kernel -- a per-lane gather, or a transpose warp -- put the scale loads' latency on the
+//   MMA's path: 41 % of the fp8 rate, measured.)
 //   TMEM: one 256-column accumulator plus 16 scale columns per stage (SFA 4, SFB 8): two
 //   accumulators would take all 512 columns.  The epilogue copies the whole accumulator to
 //   registers before releasing it, so the MMA role waits only for that copy.
@@ -139,17 +142,17 @@ constexpr uint32_t kMxBHalfBytes = (kBN / 2) * kMxBK;          // 16 KiB: 128 co
 constexpr uint32_t kMxBBytes = kBN * kMxBK;                    // 32 KiB
 constexpr uint32_t kMxStageBytes = kMxABytes + kMxBBytes;      // 48 KiB
 constexpr uint32_t kMxSfAtomBytes = 512;                       // 128 rows x 4 scales
-constexpr uint32_t kMxSfStageBytes = 3 * kMxSfAtomBytes;       // SFA atom + two SFB atoms
-constexpr uint32_t kMxSfRegionBytes = (kMxStages * kMxSfStageBytes + 1023u) & ~1023u;
+constexpr uint32_t kMxAtomSetBytes = 3 * kMxSfAtomBytes;       // SFA atom + two SFB atoms
+constexpr uint32_t kMxAtomRegionBytes = (kMxStages * kMxAtomSetBytes + 1023u) & ~1023u;
 constexpr uint32_t kMxEpiSmemBytes = kEpiWarps * kEpiBufBytes; // one staging buffer per warp
 constexpr uint32_t kMxSmemBytes =
-    kSmemAlignSlack + kMxStages * kMxStageBytes + kMxSfRegionBytes + kMxEpiSmemBytes;
+    kSmemAlignSlack + kMxStages * kMxStageBytes + kMxAtomRegionBytes + kMxEpiSmemBytes;
 constexpr uint32_t kMxAccCols = kBN;                           // TMEM columns [0, 256)
 constexpr uint32_t kMxSfColsPerStage = 16;
-constexpr uint32_t kMxLoadedArrivals = 1 + 32;                 // expect_tx + one per producer lane
-static_assert(kMxSmemBytes + 256 <= 232448, "shared memory per CTA (MXFP8)");
+constexpr uint32_t kMxPackRows = 2 * kBM;                      // packed rows pad to 256
+static_assert(kMxSmemBytes + 512 <= 232448, "shared memory per CTA (MXFP8)");
 static_assert(kMxAccCols + kMxStages * kMxSfColsPerStage <= kTmemCols, "MXFP8 TMEM budget");
-static_assert(kMxBK % (4 * kMxBlock) == 0 && kMxBK == 128, "one scale word per row and stage");
+static_assert(kMxBK == 4 * kMxBlock, "one 4-byte scale word per row and k-block");
 
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;

@@ -97,7 +97,8 @@ cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
   p.M = l.M;
   p.N = l.N;
   p.K = l.K;
-  p.sf_row_bytes = l.K / kMxBlock;
+  p.sfa_blocks = l.sfa_blocks;
+  p.sfb_blocks = l.sfb_blocks;
   p.m_blocks = l.m_blocks;
   p.n_blocks = l.n_blocks;
   p.k_blocks = l.k_blocks;
@@ -164,6 +165,17 @@ cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
 cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream) {
   if (out_dtype == 0) return debug ? launch_mx<0, true>(l, stream) : launch_mx<0, false>(l, stream);
   return debug ? launch_mx<1, true>(l, stream) : launch_mx<1, false>(l, stream);
+}
+
+cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_blocks,
+                           uint32_t row_blocks, cudaStream_t stream) {
+  const uint64_t words = static_cast<uint64_t>(k_blocks) * row_blocks * kBM;
+  if (words == 0) return cudaSuccess;
+  uint64_t blocks = (words + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  mx_pack_scales_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, k_blocks, row_blocks);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {

@@ -26,8 +26,9 @@ struct GemmLaunch {
 // the block-scaled MXFP8 GEMM (one CTA per 128 x 256 tile, the single variant's schedule)
 struct MxLaunch {
   CUtensorMap tmA, tmB, tmC;
-  const void* SFA;
+  const void* SFA;   // packed scale atoms (mx_pack_scales_kernel)
   const void* SFB;
+  uint32_t sfa_blocks, sfb_blocks;   // row blocks of 128 per k-block in the packed arrays
   uint32_t M, N, K;
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units;
@@ -50,6 +51,9 @@ cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
                         cudaStream_t stream);
 // out_dtype 0 = fp16, 1 = bf16
 cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream);
+// row-major scales [rows, 4 * k_blocks] -> atoms [k_blocks][row_blocks][512]
+cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_blocks,
+                           uint32_t row_blocks, cudaStream_t stream);
 // C[0 .. bytes) = 0 (bytes a multiple of 16, C 16-byte aligned)
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream);
 // rows of 5 int32 (worker, w, bx, by, part) over the units [0, units); tiles below

@@ -3,31 +3,30 @@
 //   C[i, j] = sum_k A[i, k] 2^(SFA[i, k / 32] - 127) * B[j, k] 2^(SFB[j, k / 32] - 127)
 //
 // The second workload of "[Feature] Introduce tile scheduler #2441"
-// (examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py): TMA-load, MMA,
-// scale-factor and epilogue roles, each walking the tiles with its own
-// PersistentTileScheduler on the single iteration clock w.  Here:
-//   * warp 0, all 32 lanes: producer.  Per tile and k-block (phase = w * k_blocks + k,
-//     slot s = phase % S): lane 0 waits consumed[s], arms loaded[s] with the operand bytes
-//     and issues the TMA loads of A (128 rows x 128 bytes) and B (256 rows x 128 bytes, two
-//     boxes; one for a half-width unit); every lane gathers 4 A-row and 8 B-row scale words
-//     (4 bytes = the 4 scales of one row for this k-block) with cp.async into the stage's
-//     scale atoms and arrives on loaded[s] when they land (33 arrivals per phase);
-//   * warp 1, one lane: MMA issuer.  Per k-block: wait loaded[s], make the cp.async writes
-//     visible to the async proxy, copy the stage's three scale atoms into its TMEM scale
-//     slot (tcgen05.cp .32x128b.warpx4), issue four tcgen05.mma kind::mxf8f6f4.block_scale
-//     128 x 256 x 32 (byte id kk of each scale word for the kk-th 32-element block), and
-//     commit to consumed[s].  After the k-loop, commit to tmem_full;
+// (examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py): TMA-load, MMA and
+// epilogue roles, each walking the tiles with its own PersistentTileScheduler on the single
+// iteration clock w, with the page's scale-factor transpose done ahead of the GEMM by
+// mx_pack_scales_kernel (scales in the tcgen05.cp source layout).  Here:
+//   * warp 0, one lane: producer.  Per tile and k-block (phase p = w * k_blocks + k, slot
+//     s = p % S): wait consumed[s], arm loaded[s] with the stage's bytes, TMA-load A (128 rows
+//     x 128 bytes) and B (256 rows x 128 bytes as two boxes; one for a half-width unit), and
+//     bulk-copy the k-block's packed scale atoms (A rows m0..m0+127: 512 bytes; B rows
+//     n0..n0+255: 1 KiB, 512 bytes for a half-width unit) into the stage's atom set;
+//   * warp 1, one lane: MMA issuer.  Per k-block: wait loaded[s], copy the atoms into the
+//     stage's TMEM scale slot (tcgen05.cp .32x128b.warpx4), issue four tcgen05.mma
+//     kind::mxf8f6f4.block_scale 128 x 256 x 32 (byte id kk of each scale word for the kk-th
+//     32-element block), commit to consumed[s].  After the k-loop, commit to tmem_full;
 //   * warps 4..7: epilogue.  Wait tmem_full, copy the warp's 32 lanes x 256 columns to
-//     registers as packed output pairs, release the accumulator (tmem_empty), then stage
-//     and TMA-store 32 x 64 chunks (clipped at M and N);
+//     registers as packed output pairs, release the accumulator (tmem_empty), then stage and
+//     TMA-store 32 x 64 chunks (clipped at M and N);
 //   * warp 2 owns the TMEM allocation (512 columns: accumulator and scale slots).
-// A scale slot is rewritten only after the producer saw consumed[s] of the phase that last
-// used it, i.e. after the MMAs that read it completed.  Every wait is bounded by the same
-// watchdog as the dense kernels.
+// A TMEM scale slot is rewritten only after loaded[s] of a later phase, which the producer
+// arms only after consumed[s] of the phase that last used it.  Every wait is bounded by the
+// same watchdog as the dense kernels.
 //
 // Shared memory (1024-byte aligned): S stages of 48 KiB (A then B, both K-major with the
-// 128-byte swizzle), then S x 1536 bytes of scale atoms (SFA, SFB columns 0..127, SFB columns
-// 128..255), then one 32 x 128-byte epilogue staging buffer per epilogue warp.
+// 128-byte swizzle); S atom sets of 1536 bytes; one 32 x 128-byte epilogue staging buffer per
+// epilogue warp.
 #pragma once
 
 #include "tg_gemm_kernel.cuh"
@@ -35,10 +34,10 @@
 namespace tg {
 
 struct MxParams {
-  const uint8_t* SFA;          // [M, K / 32] E8M0
-  const uint8_t* SFB;          // [N, K / 32] E8M0
+  const uint8_t* SFA;          // packed scale atoms of A: [K / 128][row blocks of A][512]
+  const uint8_t* SFB;          // packed scale atoms of B: [K / 128][row blocks of B][512]
   uint32_t M, N, K;
-  uint32_t sf_row_bytes;       // K / 32
+  uint32_t sfa_blocks, sfb_blocks;   // row blocks (of 128) per k-block in the packed arrays
   uint32_t m_blocks, n_blocks, k_blocks, group;
   uint32_t split_from, total_units, column_major;
   uint64_t watchdog_ns;
@@ -90,10 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sA0 = sbase;                                  // + s * kMxStageBytes
-  const uint32_t sB0 = sbase + kMxABytes;                      // + s * kMxStageBytes
-  const uint32_t sSF0 = sbase + kMxStages * kMxStageBytes;     // + s * kMxSfStageBytes
-  const uint32_t sEpi = sSF0 + kMxSfRegionBytes;
+  const uint32_t sA0 = sbase;                                   // + s * kMxStageBytes
+  const uint32_t sB0 = sbase + kMxABytes;                       // + s * kMxStageBytes
+  const uint32_t sAtom0 = sbase + kMxStages * kMxStageBytes;    // + s * kMxAtomSetBytes
+  const uint32_t sEpi = sAtom0 + kMxAtomRegionBytes;
 
   const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
   const uint32_t bar_consumed = smem_u32(&ctl.consumed[0]);
@@ -104,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kMxStages; ++s) {
-      mbar_init(bar_loaded + 8u * s, kMxLoadedArrivals);
+      mbar_init(bar_loaded + 8u * s, 1);
       mbar_init(bar_consumed + 8u * s, 1);
     }
     mbar_init(bar_tmem_full, 1);
@@ -133,72 +132,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t k_blocks = p.k_blocks;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer (whole warp)
-    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
-                                  p.total_units, p.column_major);
-    sched.init(blockIdx.x);
-    uint32_t pending = 0;       // stages whose latest TMA fill may still be in flight
-    uint32_t pending_par = 0;
-    bool ok = true;
-    while (ok && sched.valid()) {
-      const uint64_t w = sched.current_iter;
-      const bool half = sched.part >= 0;
-      const uint32_t m0 = sched.m_idx * kBM;
-      const uint32_t n0 = sched.n_idx * kBN + (half ? static_cast<uint32_t>(sched.part) * (kBN / 2) : 0u);
-      const uint32_t tx_bytes = kMxABytes + (half ? kMxBHalfBytes : kMxBBytes);
-      for (uint32_t k = 0; k < p.k_blocks; ++k) {
-        const uint64_t phase = w * k_blocks + k;
-        const uint32_t s = static_cast<uint32_t>(phase % kMxStages);
-        const uint32_t par = static_cast<uint32_t>((phase / kMxStages) & 1u);
-        bool got = true;
-        if (lane == 0) got = wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, limit, kRoleProducer);
-        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
-        pending &= ~(1u << s);
-        if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
-          continue;  // injected fault: this phase is never filled
-        const uint32_t full = bar_loaded + 8u * s;
-        const int32_t kx = static_cast<int32_t>(k * kMxBK);
-        if (lane == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, gridDim.x, p.split_from,
+                                    p.total_units, p.column_major);
+      sched.init(blockIdx.x);
+      uint32_t pending = 0;       // stages whose latest operand fill may still be in flight
+      uint32_t pending_par = 0;
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint64_t w = sched.current_iter;
+        const bool half = sched.part >= 0;
+        const int32_t m0 = static_cast<int32_t>(sched.m_idx * kBM);
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
+        const uint32_t sfb_bytes = half ? kMxSfAtomBytes : 2 * kMxSfAtomBytes;
+        const uint32_t tx_bytes = kMxABytes + (half ? kMxBHalfBytes : kMxBBytes) + kMxSfAtomBytes + sfb_bytes;
+        const uint32_t ma = static_cast<uint32_t>(m0) / kBM;      // A's row block
+        const uint32_t nb = static_cast<uint32_t>(n0) / kBM;      // B's first row block
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = w * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kMxStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kMxStages) & 1u);
+          if (!wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, limit, kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          pending &= ~(1u << s);
+          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+            continue;  // injected fault: the operands of this phase are never loaded
+          const uint32_t full = bar_loaded + 8u * s;
+          const int32_t kx = static_cast<int32_t>(k * kMxBK);
           mbar_arrive_expect_tx(full, tx_bytes);
-          tma_load_2d(sA0 + s * kMxStageBytes, &tmA, full, kx, static_cast<int32_t>(m0));
-          tma_load_2d(sB0 + s * kMxStageBytes, &tmB, full, kx, static_cast<int32_t>(n0));
-          if (!half)
-            tma_load_2d(sB0 + s * kMxStageBytes + kMxBHalfBytes, &tmB, full, kx,
-                        static_cast<int32_t>(n0 + kBN / 2));
+          tma_load_2d(sA0 + s * kMxStageBytes, &tmA, full, kx, m0);
+          tma_load_2d(sB0 + s * kMxStageBytes, &tmB, full, kx, n0);
+          if (!half) tma_load_2d(sB0 + s * kMxStageBytes + kMxBHalfBytes, &tmB, full, kx, n0 + kBN / 2);
+          const uint32_t atom = sAtom0 + s * kMxAtomSetBytes;
+          bulk_load(atom, p.SFA + (static_cast<uint64_t>(k) * p.sfa_blocks + ma) * kMxSfAtomBytes,
+                    kMxSfAtomBytes, full);
+          bulk_load(atom + kMxSfAtomBytes,
+                    p.SFB + (static_cast<uint64_t>(k) * p.sfb_blocks + nb) * kMxSfAtomBytes, sfb_bytes, full);
+          pending |= 1u << s;
+          pending_par = (pending_par & ~(1u << s)) | (par << s);
         }
-        // scale words: row r of an atom at byte (r % 32) * 16 + (r / 32) * 4; rows past the
-        // matrix are zero-filled without a read (their products never reach C)
-        const uint32_t sf = sSF0 + s * kMxSfStageBytes + lane * 16u;
-        const uint64_t kofs = static_cast<uint64_t>(k) * 4u;
-#pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) {
-          const uint32_t r = m0 + lane + 32u * i;
-          const bool in = r < p.M;
-          cp_async_4(sf + 4u * i, p.SFA + (in ? static_cast<uint64_t>(r) * p.sf_row_bytes + kofs : 0u),
-                     in ? 4u : 0u);
-        }
-#pragma unroll
-        for (uint32_t i = 0; i < 8; ++i) {
-          if (half && i >= 4) break;
-          const uint32_t n = n0 + lane + 32u * i;
-          const bool in = n < p.N;
-          cp_async_4(sf + kMxSfAtomBytes * (1u + i / 4u) + 4u * (i % 4u),
-                     p.SFB + (in ? static_cast<uint64_t>(n) * p.sf_row_bytes + kofs : 0u), in ? 4u : 0u);
-        }
-        cp_async_mbar_arrive(full);
-        pending |= 1u << s;
-        pending_par = (pending_par & ~(1u << s)) | (par << s);
+        sched.next_tile();
       }
-      sched.next_tile();
-    }
-    cp_async_wait_all();
-    if (!ok && lane == 0) {
-      for (uint32_t s = 0; s < kMxStages; ++s)
-        if ((pending >> s) & 1u)
-          wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+      if (!ok) {
+        for (uint32_t s = 0; s < kMxStages; ++s)
+          if ((pending >> s) & 1u)
+            wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -226,12 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tcgen05_fence_after_sync();
-          fence_proxy_async_shared();   // the cp.async scale writes, for tcgen05.cp
-          const uint32_t sf = sSF0 + s * kMxSfStageBytes;
+          const uint32_t atom = sAtom0 + s * kMxAtomSetBytes;
           const uint32_t t_sf = tmem_base + kMxAccCols + s * kMxSfColsPerStage;
-          tmem_cp_32x128b_x4(t_sf, smem_desc_plain(sf, 128, 128));
-          tmem_cp_32x128b_x4(t_sf + 4, smem_desc_plain(sf + kMxSfAtomBytes, 128, 128));
-          if (!half) tmem_cp_32x128b_x4(t_sf + 8, smem_desc_plain(sf + 2 * kMxSfAtomBytes, 128, 128));
+          tmem_cp_32x128b_x4(t_sf, smem_desc_plain(atom, 128, 128));
+          tmem_cp_32x128b_x4(t_sf + 4, smem_desc_plain(atom + kMxSfAtomBytes, 128, 128));
+          if (!half) tmem_cp_32x128b_x4(t_sf + 8, smem_desc_plain(atom + 2 * kMxSfAtomBytes, 128, 128));
           const uint32_t a_addr = sA0 + s * kMxStageBytes;
           const uint32_t b_addr = sB0 + s * kMxStageBytes;
 #pragma unroll
@@ -307,6 +288,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tcgen05_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Packs row-major scales sf [rows, K / 32] into atoms: out[(k * row_blocks + b) * 512 +
+// (r % 32) * 16 + (r / 32) * 4 + j] = sf[b * 128 + r, 4k + j] (0 for rows >= rows), for every
+// k-block k < K / 128, row block b < row_blocks and r < 128.  One thread per 4-byte word.
+__global__ void mx_pack_scales_kernel(const uint8_t* __restrict__ sf, uint8_t* __restrict__ out,
+                                      uint32_t rows, uint32_t k_blocks, uint32_t row_blocks) {
+  const uint64_t words = static_cast<uint64_t>(k_blocks) * row_blocks * kBM;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  const uint64_t row_bytes = static_cast<uint64_t>(k_blocks) * 4u;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+       i += stride) {
+    const uint32_t r = static_cast<uint32_t>(i % kBM);
+    const uint64_t kb = i / kBM;                    // k * row_blocks + b
+    const uint32_t b = static_cast<uint32_t>(kb % row_blocks);
+    const uint32_t k = static_cast<uint32_t>(kb / row_blocks);
+    const uint32_t row = b * kBM + r;
+    const uint32_t v = row < rows ? *reinterpret_cast<const uint32_t*>(sf + row * row_bytes + 4u * k) : 0u;
+    *reinterpret_cast<uint32_t*>(out + kb * kMxSfAtomBytes + (r % 32u) * 16u + (r / 32u) * 4u) = v;
   }
 }
 

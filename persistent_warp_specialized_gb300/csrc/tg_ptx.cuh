@@ -233,22 +233,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 
 // ---------------------------------------------------------------- block-scaled MMA (MXFP8)
-// 4-byte global -> shared copy (cp.async, L1-allocating); ``src_bytes`` 0 writes zeros and
-// reads nothing.  Both addresses 4-byte aligned.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-// Arrive on ``bar`` once every cp.async this thread issued so far has landed; the arrival
-// counts against the barrier's expected count (noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
+// Contiguous global -> shared copy of ``bytes`` (a multiple of 16; both addresses 16-byte
+// aligned) by the bulk-copy engine, completing ``bytes`` transaction bytes on ``bar``.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // Shared -> TMEM copy of a 32-row x 16-byte matrix into all four 32-lane quadrants: lane

@@ -101,7 +101,7 @@ def test_mxfp8_host_side_rejections_need_no_gpu(lib):
         ((16, 16, 16, 16, 16, 8, 12, 128, "bf16"), tg.TG_ERR_ALIGN),  # N % 8 != 0
         ((16, 16, None, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ARG),  # null B
         ((16, 16, 16, None, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ARG),  # null SFB
-        ((16, 18, 16, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ALIGN),  # SFA not 4-byte aligned
+        ((16, 24, 16, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ALIGN),  # SFA not 16-byte aligned
         ((24, 16, 16, 16, 16, 8, 8, 128, "bf16"), tg.TG_ERR_ALIGN),  # A not 16-byte aligned
     ]
     for args, code in cases:
@@ -113,3 +113,26 @@ def test_mxfp8_host_side_rejections_need_no_gpu(lib):
     assert rc == tg.TG_ERR_ARG
     assert tg.tg_gemm_mxfp8(None, None, None, None, None, 0, 8, 128, "bf16", stream=0) == 0
     assert tg.tg_gemm_mxfp8(None, None, None, None, None, 8, 0, 128, "bf16", stream=0) == 0
+
+
+def test_mxfp8_packed_scale_sizes_and_rejections(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    # k-blocks x row blocks (rows padded to a multiple of 256) x 512 bytes
+    assert tg.tg_mxfp8_scale_bytes(0, 128) == 0
+    assert tg.tg_mxfp8_scale_bytes(1, 128) == 1 * 2 * 512
+    assert tg.tg_mxfp8_scale_bytes(256, 128) == 1 * 2 * 512
+    assert tg.tg_mxfp8_scale_bytes(257, 256) == 2 * 4 * 512
+    assert tg.tg_mxfp8_scale_bytes(8192, 8192) == 64 * 64 * 512
+    for args, code in [((-1, 128), tg.TG_ERR_ARG), ((8, 96), tg.TG_ERR_ALIGN)]:
+        with pytest.raises(tg.TgError) as e:
+            tg.tg_mxfp8_scale_bytes(*args)
+        assert e.value.code == code
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_mxfp8_pack_scales(16, None, 8, 128, stream=0)        # null output
+    assert e.value.code == tg.TG_ERR_ARG
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_mxfp8_pack_scales(16, 24, 8, 128, stream=0)          # output not 16-byte aligned
+    assert e.value.code == tg.TG_ERR_ALIGN
+    assert tg.tg_mxfp8_pack_scales(None, None, 0, 0, stream=0) == 0

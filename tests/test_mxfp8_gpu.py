@@ -27,11 +27,17 @@ def _lib():
     ensure_library()
 
 
+def device_inputs(a, sa, b, sb):
+    """Device copies of A and B and the packed device scales of SA and SB."""
+    K = a.shape[1]
+    return a.cuda(), tg.mxfp8_pack(sa.cuda(), K), b.cuda(), tg.mxfp8_pack(sb.cuda(), K)
+
+
 def run_mx(a, sa, b, sb, out="bf16", debug=False, **kw):
     M, K = a.shape
     N = b.shape[0]
     c = nan_filled(M, N, out)
-    dev = [t.cuda() for t in (a, sa, b, sb)]
+    dev = device_inputs(a, sa, b, sb)
     if debug:
         tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, out, **kw)
     else:
@@ -60,6 +66,32 @@ def check_tolerance(c_bits, r_bits, a, sa, b, sb, out, what, gate=True):
     bound = 2.0 * formats.ulp(r_bits, out) + K * u / (1 - K * u) * s
     bad = err > bound
     assert not bad.any(), f"{what}: {int(bad.sum())} outside the fp32 accumulation bound"
+
+
+def packed_layout(sf, K):
+    """The packed layout as the C header defines it, written out element by element."""
+    rows = sf.shape[0]
+    row_blocks = 2 * ((rows + 255) // 256)
+    out = np.zeros((K // 128) * row_blocks * 512, np.uint8)
+    for k in range(K // 128):
+        for b in range(row_blocks):
+            for r in range(128):
+                if b * 128 + r < rows:
+                    for j in range(4):
+                        out[(k * row_blocks + b) * 512 + (r % 32) * 16 + (r // 32) * 4 + j] = \
+                            sf[b * 128 + r, 4 * k + j]
+    return out
+
+
+@pytest.mark.parametrize("rows,K", [(1, 128), (128, 256), (300, 384), (513, 512), (256, 128)])
+def test_pack_scales_is_the_documented_layout(rows, K):
+    gen = torch.Generator().manual_seed(rows + K)
+    sf = torch.randint(0, 256, (rows, K // 32), generator=gen).to(torch.uint8)
+    packed = torch.full((tg.tg_mxfp8_scale_bytes(rows, K),), 0xAB, dtype=torch.uint8,
+                        device="cuda")
+    tg.tg_mxfp8_pack_scales(sf.cuda(), packed, rows, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), packed_layout(sf.numpy(), K))
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (512, 768, 512), (1000, 520, 384),
@@ -116,7 +148,7 @@ def test_kernel_followed_the_schedule(M, N, K, plain, column_major):
 def test_watchdog_fires_and_context_survives():
     M, N, K = 512, 512, 1024
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=1)
-    dev = [t.cuda() for t in (a, sa, b, sb)]
+    dev = device_inputs(a, sa, b, sb)
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tg.TgError) as e:
         tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, "bf16", watchdog_ns=20_000_000,
@@ -128,7 +160,7 @@ def test_watchdog_fires_and_context_survives():
 
 def test_empty_and_zero_k():
     c = nan_filled(64, 64, "bf16")
-    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")   # K = 0: nothing is read
     assert tg.tg_gemm_mxfp8(z, z, z, z, c, 64, 64, 0, "bf16") == 0
     torch.cuda.synchronize()
     assert (c.float() == 0).all()

@@ -248,3 +248,114 @@ def test_response_ring_numbered_from_one_is_caught():
     # once on a fresh barrier, so a reader takes a response that was never written
     failures = [run_response_ring(2, 6, 3, seed, first=1) for seed in range(40)]
     assert all(f is not None for f in failures)
+
+
+# ---------------------------------------------------------------- MXFP8 scale path
+# The block-scaled kernel's roles: the producer arms loaded[s] (expect_tx, one arrival) and its
+# TMA bytes land later; the transpose role waits atom_free[a] (a = phase % A) for the phase
+# that last used the slot, writes the atoms and arrives on sf_ready[a]; the MMA role waits
+# loaded[s] and sf_ready[a], reads both, and commits consumed[s] and atom_free[a].  The model
+# tracks each barrier's pending arrivals and transaction bytes, so a phase that completes
+# before the producer armed it is seen.  ``shared_loaded`` is the design that failed on the
+# GPU: the transpose arriving on loaded[s] (count 2) instead of a barrier of its own, which
+# lets it complete phase p of loaded[s] early once it runs S or more phases ahead.
+
+
+class TxBarrier(Barrier):
+    def __init__(self, count):
+        super().__init__()
+        self.count = count
+        self.pending = count
+        self.tx = 0
+        self.armed = False
+
+    def arrive(self, expect_tx=0, armed=False):
+        self.tx += expect_tx
+        self.armed = self.armed or armed
+        self.pending -= 1
+        return self._check()
+
+    def land(self, nbytes):
+        self.tx -= nbytes
+        return self._check()
+
+    def _check(self):
+        if self.pending == 0 and self.tx == 0:
+            early = not self.armed
+            self.pending = self.count
+            self.armed = False
+            self.complete()
+            return "early" if early else "ok"
+        return None
+
+
+def run_mx_scales(S, A, k_total, seed, shared_loaded=False):
+    rng = random.Random(seed)
+    loaded = [TxBarrier(2 if shared_loaded else 1) for _ in range(S)]
+    consumed = [Barrier() for _ in range(S)]
+    sf_ready = [Barrier() for _ in range(A)]
+    atom_free = [Barrier() for _ in range(A)]
+    stage = [None] * S          # phase whose operands sit in stage s
+    atoms = [None] * A          # phase whose scales sit in atom slot a
+    in_flight = []              # (stage, phase) TMA fills not landed yet
+    prod = tr = mma = 0
+    while mma < k_total:
+        moves = []
+        if prod < k_total and consumed[prod % S].passes(((prod // S) & 1) ^ 1):
+            moves.append("p")
+        if in_flight:
+            moves.append("land")
+        if tr < k_total and (tr < A or atom_free[tr % A].passes(((tr // A) & 1) ^ 1)):
+            moves.append("t")
+        s, a = mma % S, mma % A
+        ready = loaded[s].passes((mma // S) & 1)
+        if not shared_loaded:
+            ready = ready and sf_ready[a].passes((mma // A) & 1)
+        if ready:
+            moves.append("m")
+        if not moves:
+            return f"deadlock: producer {prod}, transpose {tr}, mma {mma}"
+        mv = rng.choice(moves)
+        if mv == "p":
+            s = prod % S
+            if loaded[s].arrive(expect_tx=1, armed=True) == "early":
+                return f"loaded[{s}] completed before phase {prod} was armed"
+            in_flight.append((s, prod))
+            prod += 1
+        elif mv == "land":
+            s, ph = in_flight.pop(rng.randrange(len(in_flight)))
+            stage[s] = ph
+            if loaded[s].land(1) == "early":
+                return f"loaded[{s}] completed early (phase {ph})"
+        elif mv == "t":
+            a = tr % A
+            atoms[a] = tr
+            if shared_loaded:
+                if loaded[tr % S].arrive() == "early":
+                    return f"loaded[{tr % S}] completed before phase {tr} was armed"
+            else:
+                sf_ready[a].complete()
+            tr += 1
+        else:
+            s, a = mma % S, mma % A
+            if stage[s] != mma:
+                return f"MMA phase {mma} read the operands of phase {stage[s]}"
+            if atoms[a] != mma:
+                return f"MMA phase {mma} read the scales of phase {atoms[a]}"
+            consumed[s].complete()
+            atom_free[a].complete()
+            mma += 1
+    return None
+
+
+@pytest.mark.parametrize("S,A", [(4, 8), (4, 4), (4, 3), (3, 8), (2, 5)])
+def test_mx_scale_path_holds(S, A):
+    for seed in range(150):
+        assert run_mx_scales(S, A, 40, seed) is None, (S, A, seed)
+
+
+def test_mx_scales_arriving_on_loaded_are_caught():
+    # 8 atom slots let the transpose role run 7 phases ahead: with its arrival on loaded[s],
+    # some interleaving completes a phase of loaded[s] before the producer armed it
+    failures = [run_mx_scales(4, 8, 40, seed, shared_loaded=True) for seed in range(150)]
+    assert any(f is not None for f in failures)
