@@ -202,7 +202,7 @@ def parse_clock_csv(lines, t0, t1):
 
 def profile_traffic(kernel, workload):
     """DRAM bytes per launch of ``kernel`` on ``workload`` from its committed ncu summary
-    (profiles/<kernel>_<size>_<dtype>.md), or None if there is none or the library's sources
+    (profiles/<kernel>_<size>_<dtype>.md), or None if there is none or the kernel's sources
     changed since that capture."""
     from persistent_warp_specialized_gb300 import _build
 
@@ -217,7 +217,7 @@ def profile_traffic(kernel, workload):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip().strip("`")] = v.strip().strip("`")
-    if vals.get("source_stamp") != _build._stamp():
+    if vals.get("source_stamp") != _build.kernel_stamp(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -335,7 +335,7 @@ def run_tg(args):
 
     _build.build()
     tg.load_library()
-    w = wl.WORKLOADS[args.workload]
+    w = {**wl.WORKLOADS, **wl.PROFILE_WORKLOADS}[args.workload]
     a_cpu, b_cpu = wl.workload_inputs(w)
     a = a_cpu.to(dev)
     b = b_cpu.to(dev)
@@ -451,8 +451,8 @@ def mx_oracle_slab(a, sa, b, sb, rows):
     return mx.gemm_mxfp8_ref(a[:rows], sa[:rows], b, sb, "bf16")
 
 
-def mx_config(M, N, K, seed):
-    return {"workload": "mxfp8_8192", "M": M, "N": N, "K": K, "in_dtype": "e4m3",
+def mx_config(name, M, N, K, seed):
+    return {"workload": name, "M": M, "N": N, "K": K, "in_dtype": "e4m3",
             "scale": "e8m0 per 32 K-elements of each A row and B column", "out_dtype": "bf16",
             "accumulate": "fp32", "inputs": f"MX-quantized N(0,1) / N(0,1/K) draws, seed {seed}",
             "l2": "inputs larger than L2 (no flush)",
@@ -487,7 +487,7 @@ def run_reference_mx(args):
         "impl": "reference", "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": mx_config(M, N, K, seed),
+        "config": mx_config(args.workload, M, N, K, seed),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -574,7 +574,7 @@ def run_tg_mx(args):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                 "frac": achieved / peak, "kernel": "gemm_mxfp8_ws",
                 "kernel_ms": gemm_ms,
-                "traffic": profile_traffic("gemm_mxfp8_ws", "8192_mxfp8"),
+                "traffic": profile_traffic("gemm_mxfp8_ws", f"{M}_mxfp8"),
                 "peak_source": f"{peak_src}: bf16 burst peak x 2 (the nominal dense fp8 / bf16 "
                                f"ratio, 4.5 / 2.25 PFLOP/s)",
                 "frac_of_nominal_dense": achieved / (2 * NOMINAL_DENSE_BF16_TFLOPS),
@@ -583,7 +583,7 @@ def run_tg_mx(args):
         "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; see config.inputs)",
-        "config": dict(mx_config(M, N, K, seed), sms=sms),
+        "config": dict(mx_config(args.workload, M, N, K, seed), sms=sms),
         "gpu_launches": 3 * steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

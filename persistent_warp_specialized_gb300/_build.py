@@ -53,6 +53,29 @@ def _stamp():
     return h.hexdigest()
 
 
+# The sources each GEMM kernel's device code is built from (a profile taken of a kernel stays
+# valid while these and the flags are unchanged).
+KERNEL_SOURCES = {
+    "gemm_persistent_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh",
+                           "tg_gemm_kernel.cuh"],
+    "gemm_pair_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
+                     "tg_gemm_pair_kernel.cuh"],
+    "gemm_mxfp8_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
+                      "tg_mx_kernel.cuh"],
+}
+
+
+def kernel_stamp(kernel):
+    """sha256 of one kernel's device sources and the flags."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(FLAGS).encode())
+    return h.hexdigest()
+
+
 def build(force=False, verbose=False, ptxas_info=False):
     """Compile libtg.so if its sources changed; returns its path."""
     stamp = _stamp()

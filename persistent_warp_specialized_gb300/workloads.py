@@ -41,6 +41,11 @@ WORKLOADS = {
     )
 }
 
+# A smaller case of the 8192^3 kernel for detailed profiles (inputs still larger than L2).
+PROFILE_WORKLOADS = {
+    w.name: w for w in (Workload("gemm_6144_bf16", 6144, 6144, 6144, "bf16", "normal", 7),)
+}
+
 # number of workers and group width the tile schedule of the 256^3 workload is checked with
 SCHEDULE_CHECK_WORKERS = 148
 SCHEDULE_CHECK_GROUP = 8
@@ -90,6 +95,7 @@ def bits(t):
 # add small, ragged and integer-valued cases.
 MX_WORKLOADS = {
     "mxfp8_8192": (8192, 8192, 8192, 6),   # M, N, K, seed
+    "mxfp8_6144": (6144, 6144, 6144, 8),   # a smaller case for detailed profiles
 }
 MX_BLOCK = 32
 
