@@ -456,7 +456,8 @@ def mx_config(name, M, N, K, seed):
             "scale": "e8m0 per 32 K-elements of each A row and B column", "out_dtype": "bf16",
             "accumulate": "fp32", "inputs": f"MX-quantized N(0,1) / N(0,1/K) draws, seed {seed}",
             "l2": "inputs larger than L2 (no flush)",
-            "tile": "128 x 256 x 128 bytes, 4 stages; persistent: one CTA per SM",
+            "tile": "CTA pair: 256 x 256 x 128 bytes, 6 stages (single CTA: 128 x 256, 4 stages); "
+                    "persistent",
             "step": "pack both operands' scales (2 launches) + the GEMM (1 launch)"}
 
 
@@ -531,6 +532,9 @@ def run_tg_mx(args):
     def gemm_only():
         tg.tg_gemm_mxfp8(a, sa_p, b, sb_p, c, M, N, K, "bf16", stream)
 
+    launch = tg.tg_gemm_launch_shape(M, N, K, "auto")   # tg_gemm_mxfp8 chooses as this does
+    kernel = "gemm_mxfp8_pair_ws" if launch["variant"] == tg.TG_VARIANT_PAIR else "gemm_mxfp8_ws"
+
     steps, warm = max(1, args.steps), max(3, args.warmup)
     ms_local, ms, clocks = timed_region(step, steps, warm, dev, stream, world)
     value = world * flops / (ms * 1e-3) / 1e12
@@ -572,9 +576,9 @@ def run_tg_mx(args):
     achieved = flops / (gemm_ms * 1e-3) / 1e12    # the GEMM kernel alone
     peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "kernel": "gemm_mxfp8_ws",
+                "frac": achieved / peak, "kernel": kernel,
                 "kernel_ms": gemm_ms,
-                "traffic": profile_traffic("gemm_mxfp8_ws", f"{M}_mxfp8"),
+                "traffic": profile_traffic(kernel, f"{M}_mxfp8"),
                 "peak_source": f"{peak_src}: bf16 burst peak x 2 (the nominal dense fp8 / bf16 "
                                f"ratio, 4.5 / 2.25 PFLOP/s)",
                 "frac_of_nominal_dense": achieved / (2 * NOMINAL_DENSE_BF16_TFLOPS),
@@ -583,7 +587,7 @@ def run_tg_mx(args):
         "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; see config.inputs)",
-        "config": dict(mx_config(args.workload, M, N, K, seed), sms=sms),
+        "config": dict(mx_config(args.workload, M, N, K, seed), sms=sms, launch=launch),
         "gpu_launches": 3 * steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -220,17 +220,25 @@ int tg_mxfp8_pack_scales(const void* sf_dev, void* packed_dev, int64_t rows, int
  *   M, N, K >= 0 and < 2^31; K % 128 == 0; N % 8 == 0.  All five pointers 16-byte aligned.
  *   C must not overlap any input.  M == 0 or N == 0: nothing is done.  K == 0: C is
  *   zero-filled.
- * The launch is that of TG_VARIANT_SINGLE (tg_gemm_launch_shape): one persistent CTA per SM,
- * 128 x 256 output tiles, grouped order with the tail split.  Asynchronous; errors as for
- * tg_gemm_persistent.  Inputs that hold NaN patterns give unspecified outputs.
+ * Kernels: one CTA per 128 x 256 output tile (TG_VARIANT_SINGLE), or a CTA pair per 256 x 256
+ * tile (TG_VARIANT_PAIR, tcgen05 cta_group::2); tg_gemm_mxfp8 chooses as TG_VARIANT_AUTO does
+ * for tg_gemm_persistent, and tg_gemm_launch_shape gives the launch of either.  Persistent,
+ * grouped order with the tail split.  Asynchronous; errors as for tg_gemm_persistent.
+ * Inputs that hold NaN patterns give unspecified outputs.
  */
 int tg_gemm_mxfp8(const void* A_dev, const void* SFA_dev, const void* B_dev, const void* SFB_dev,
                   void* C_dev, int64_t M, int64_t N, int64_t K, int out_dtype, void* stream);
 
+/* tg_gemm_mxfp8 with an explicit kernel: variant TG_VARIANT_AUTO, _SINGLE or _PAIR, optionally
+   OR'ed with TG_SCHEDULE_PLAIN and/or TG_SCHEDULE_COLUMN_MAJOR (others: TG_ERR_ARG). */
+int tg_gemm_mxfp8_ex(const void* A_dev, const void* SFA_dev, const void* B_dev,
+                     const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,
+                     int out_dtype, void* stream, int variant);
+
 /*
- * tg_gemm_mxfp8_debug -- tg_gemm_mxfp8, synchronously, with the inspection aids of
+ * tg_gemm_mxfp8_debug -- tg_gemm_mxfp8_ex, synchronously, with the inspection aids of
  * tg_gemm_persistent_debug (trace of 5 int32 per unit, watchdog limit, injected missing fill).
- *   flags: 0, or TG_SCHEDULE_PLAIN and/or TG_SCHEDULE_COLUMN_MAJOR (others: TG_ERR_ARG).
+ *   flags: as tg_gemm_mxfp8_ex's variant.
  */
 int tg_gemm_mxfp8_debug(const void* A_dev, const void* SFA_dev, const void* B_dev,
                         const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,

@@ -45,6 +45,7 @@ EXPORTED = (
     "tg_device_status",
     "tg_gemm_persistent_host",
     "tg_gemm_mxfp8",
+    "tg_gemm_mxfp8_ex",
     "tg_gemm_mxfp8_debug",
     "tg_mxfp8_scale_bytes",
     "tg_mxfp8_pack_scales",
@@ -94,6 +95,8 @@ def load_library(path=LIB_PATH):
     lib.tg_gemm_persistent_host.restype = i32
     lib.tg_gemm_mxfp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.tg_gemm_mxfp8.restype = i32
+    lib.tg_gemm_mxfp8_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32]
+    lib.tg_gemm_mxfp8_ex.restype = i32
     lib.tg_gemm_mxfp8_debug.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
                                         i64]
     lib.tg_gemm_mxfp8_debug.restype = i32
@@ -220,8 +223,9 @@ def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True, col
     return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
 
 
-def _mx_flags(plain=False, column_major=False):
-    return (TG_SCHEDULE_PLAIN if plain else 0) | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
+def _mx_flags(variant="auto", plain=False, column_major=False):
+    return (VARIANTS[variant] | (TG_SCHEDULE_PLAIN if plain else 0)
+            | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0))
 
 
 def tg_mxfp8_scale_bytes(rows, K):
@@ -251,11 +255,19 @@ def tg_gemm_mxfp8(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None):
         _stream(stream)))
 
 
+def tg_gemm_mxfp8_ex(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None, variant="auto",
+                     plain=False, column_major=False):
+    return _check(load_library().tg_gemm_mxfp8_ex(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
+        _stream(stream), _mx_flags(variant, plain, column_major)))
+
+
 def tg_gemm_mxfp8_debug(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None, trace=None,
-                        watchdog_ns=0, inject_skip_phase=-1, plain=False, column_major=False):
+                        watchdog_ns=0, inject_skip_phase=-1, variant="auto", plain=False,
+                        column_major=False):
     return _check(load_library().tg_gemm_mxfp8_debug(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
-        _stream(stream), _mx_flags(plain, column_major), _ptr(trace), watchdog_ns,
+        _stream(stream), _mx_flags(variant, plain, column_major), _ptr(trace), watchdog_ns,
         inject_skip_phase))
 
 

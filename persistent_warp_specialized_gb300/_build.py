@@ -62,6 +62,9 @@ KERNEL_SOURCES = {
                      "tg_gemm_pair_kernel.cuh"],
     "gemm_mxfp8_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
                       "tg_mx_kernel.cuh"],
+    "gemm_mxfp8_pair_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh",
+                           "tg_gemm_kernel.cuh", "tg_gemm_pair_kernel.cuh", "tg_mx_kernel.cuh",
+                           "tg_mx_pair_kernel.cuh"],
 }
 
 

@@ -116,10 +116,10 @@ bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
 }
 
 // A row-major [outer, inner] matrix of ``elem_bytes``-byte elements, boxes of
-// box_outer rows x box_inner elements landing with the 128-byte swizzle.
+// box_outer rows x box_inner elements landing with the 128-byte swizzle (or none).
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t elem_bytes, const void* base,
                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                 const char* name) {
+                 const char* name, bool swizzle = true) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   const cuuint64_t dims[2] = {inner, outer};
@@ -127,7 +127,8 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t elem_bytes, 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
@@ -337,13 +338,17 @@ int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, 
 int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M,
             int64_t N, int64_t K, int out_dtype, void* stream, int flags, bool debug,
             int32_t* trace, uint64_t watchdog_ns, int64_t inject) {
-  if (flags & ~(TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR))
-    return fail(TG_ERR_ARG, "unknown MXFP8 schedule flags 0x%x", flags);
+  int variant = flags & ~(TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR);
+  if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
+    return fail(TG_ERR_ARG, "unknown MXFP8 variant or schedule flags 0x%x", flags);
   bool nothing = false;
   int rc = validate_mx(A, SFA, B, SFB, C, M, N, K, out_dtype, &nothing);
   if (rc != TG_OK || nothing) return rc;
   int sms = 0, max_pairs = 0;
   if ((rc = device_ready(&sms, &max_pairs)) != TG_OK) return rc;
+  if (variant == TG_VARIANT_AUTO) variant = auto_variant(M, N, K, max_pairs);
+  if (variant == TG_VARIANT_PAIR && max_pairs < 1)
+    return fail(TG_ERR_CUDA, "no CTA pair of the MXFP8 pair kernel fits on this device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) {
     cudaError_t e = tg::launch_zero_fill(C, uint64_t(M) * N * tg::kElemBytes, s);
@@ -359,8 +364,22 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
   if ((rc = encode_2d(&l.tmC, out_dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
   l.sfa_blocks = static_cast<uint32_t>(mx_row_blocks(M));
   l.sfb_blocks = static_cast<uint32_t>(mx_row_blocks(N));
-  const Shape sh = launch_shape(M, N, K, TG_VARIANT_SINGLE, (flags & TG_SCHEDULE_PLAIN) != 0,
-                                false, sms, max_pairs);
+  if (variant == TG_VARIANT_PAIR) {
+    // the packed scales as rows of 128 32-bit words, one row per atom: one atom of A and two
+    // adjacent atoms of B per box
+    const uint64_t k_blocks = uint64_t(K) / tg::kMxBK;
+    if ((rc = encode_tiled(&l.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, SFA, 128,
+                           k_blocks * l.sfa_blocks, 128, 1, "SFA", false)) != TG_OK)
+      return rc;
+    if ((rc = encode_tiled(&l.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, SFB, 128,
+                           k_blocks * l.sfb_blocks, 128, 2, "SFB", false)) != TG_OK)
+      return rc;
+  } else {
+    l.tmSFA = l.tmA;   // unused by the single-CTA kernel
+    l.tmSFB = l.tmA;
+  }
+  const Shape sh = launch_shape(M, N, K, variant, (flags & TG_SCHEDULE_PLAIN) != 0, false, sms,
+                                max_pairs);
   l.SFA = SFA;
   l.SFB = SFB;
   l.M = static_cast<uint32_t>(M);
@@ -380,7 +399,7 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
   cudaError_t e;
   if (debug && (e = tg::clear_watchdog_status(s)) != cudaSuccess)
     return fail_cuda("clearing the watchdog word", e);
-  if ((e = tg::launch_mxfp8(out_dtype, debug, l, s)) != cudaSuccess)
+  if ((e = tg::launch_mxfp8(out_dtype, debug, variant, l, s)) != cudaSuccess)
     return fail_cuda("MXFP8 GEMM launch", e);
   if (debug) {
     unsigned int st = 0;
@@ -432,6 +451,13 @@ int tg_mxfp8_pack_scales(const void* sf_dev, void* packed_dev, int64_t rows, int
 int tg_gemm_mxfp8(const void* A_dev, const void* SFA_dev, const void* B_dev, const void* SFB_dev,
                   void* C_dev, int64_t M, int64_t N, int64_t K, int out_dtype, void* stream) {
   return mx_impl(A_dev, SFA_dev, B_dev, SFB_dev, C_dev, M, N, K, out_dtype, stream, 0, false,
+                 nullptr, 0, -1);
+}
+
+int tg_gemm_mxfp8_ex(const void* A_dev, const void* SFA_dev, const void* B_dev,
+                     const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,
+                     int out_dtype, void* stream, int variant) {
+  return mx_impl(A_dev, SFA_dev, B_dev, SFB_dev, C_dev, M, N, K, out_dtype, stream, variant, false,
                  nullptr, 0, -1);
 }
 

@@ -154,6 +154,36 @@ static_assert(kMxSmemBytes + 512 <= 232448, "shared memory per CTA (MXFP8)");
 static_assert(kMxAccCols + kMxStages * kMxSfColsPerStage <= kTmemCols, "MXFP8 TMEM budget");
 static_assert(kMxBK == 4 * kMxBlock, "one 4-byte scale word per row and k-block");
 
+// CTA-pair MXFP8 kernel (tcgen05 cta_group::2; the page's example is 2-CTA): a cluster of two
+// CTAs computes a 256 x 256 output tile.  CTA r loads A rows [128r, 128r + 128) and B rows
+// (N) [128r, 128r + 128) of the tile (for a 128-wide half unit: [64r, 64r + 128), of which the
+// MMA reads 64), its own SFA atom and both SFB atoms, by TMA completing on the even CTA's
+// barrier; the even CTA copies the atoms into both CTAs' TMEM (tcgen05.cp .cta_group::2 copies
+// each CTA's shared memory into its own TMEM, measured) and issues 256 x 256 x 32 MMAs.  Half
+// of B per CTA makes a k-block 32 KiB; stages of two k-blocks (eight MMAs per hand-over, three
+// stages) ran faster than six stages of one.
+// A stage holds TG_MX_PAIR_KB k-blocks of 128 (each: 16 KiB of A, 16 KiB of B, 1.5 KiB of
+// atoms per CTA); a K tail leaves the last stage partly zero-filled by TMA.
+#ifndef TG_MX_PAIR_KB
+#define TG_MX_PAIR_KB 2
+#endif
+#ifndef TG_MX_PAIR_STAGES
+#define TG_MX_PAIR_STAGES (6 / TG_MX_PAIR_KB)
+#endif
+constexpr int kMxPairKB = TG_MX_PAIR_KB;
+constexpr int kMxPairStages = TG_MX_PAIR_STAGES;
+constexpr uint32_t kMxPairBBytes = (kBN / 2) * kMxBK;              // 16 KiB: 128 rows of B
+constexpr uint32_t kMxPairKbBytes = kMxABytes + kMxPairBBytes;     // 32 KiB per k-block
+constexpr uint32_t kMxPairStageBytes = kMxPairKB * kMxPairKbBytes;  // A blocks, then B blocks
+constexpr uint32_t kMxPairTxBytes = 2 * kMxPairKB * (kMxPairKbBytes + kMxAtomSetBytes);
+constexpr uint32_t kMxPairAtomRegionBytes =
+    (kMxPairStages * kMxPairKB * kMxAtomSetBytes + 1023u) & ~1023u;
+constexpr uint32_t kMxPairSmemBytes = kSmemAlignSlack + kMxPairStages * kMxPairStageBytes +
+                                      kMxPairAtomRegionBytes + kMxEpiSmemBytes;
+static_assert(kMxPairSmemBytes + 512 <= 232448, "shared memory per CTA (MXFP8 pair)");
+static_assert(kMxAccCols + kMxPairStages * kMxPairKB * kMxSfColsPerStage <= kTmemCols,
+              "MXFP8 pair TMEM budget");
+
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;
 constexpr uint32_t kRoleMma = 2u;

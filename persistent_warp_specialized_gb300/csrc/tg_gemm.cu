@@ -1,11 +1,12 @@
 // tg_gemm.cu -- instantiations and launchers of the sm_103a kernels behind the C ABI:
 // the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
-// block-scaled MXFP8 GEMM, the tile-schedule inspection kernel, and the zero fill used when
+// block-scaled MXFP8 GEMM (single CTA and CTA pair), the tile-schedule inspection kernel, and the zero fill used when
 // K == 0.  All kernels share this translation unit's watchdog status word.
 #include "tg_gemm_kernel.cuh"
 #include "tg_gemm_pair_kernel.cuh"
 #include "tg_internal.h"
 #include "tg_mx_kernel.cuh"
+#include "tg_mx_pair_kernel.cuh"
 
 namespace tg {
 
@@ -89,8 +90,7 @@ cudaError_t set_smem_attr() {
                               static_cast<int>(kPairSmemBytes));
 }
 
-template <int OUT, bool DEBUG>
-cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
+MxParams mx_params_of(const MxLaunch& l) {
   MxParams p;
   p.SFA = static_cast<const uint8_t*>(l.SFA);
   p.SFB = static_cast<const uint8_t*>(l.SFB);
@@ -109,16 +109,32 @@ cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
   p.inject_skip_phase = l.inject_skip_phase;
-  gemm_mxfp8_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxSmemBytes, stream>>>(l.tmA, l.tmB,
-                                                                                l.tmC, p);
+  return p;
+}
+
+template <int OUT, bool DEBUG>
+cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
+  gemm_mxfp8_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxSmemBytes, stream>>>(
+      l.tmA, l.tmB, l.tmC, mx_params_of(l));
+  return cudaGetLastError();
+}
+
+template <int OUT, bool DEBUG>
+cudaError_t launch_mx_pair(const MxLaunch& l, cudaStream_t stream) {
+  gemm_mxfp8_pair_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxPairSmemBytes, stream>>>(
+      l.tmA, l.tmB, l.tmC, l.tmSFA, l.tmSFB, mx_params_of(l));
   return cudaGetLastError();
 }
 
 template <int OUT, bool DEBUG>
 cudaError_t set_mx_smem_attr() {
-  return cudaFuncSetAttribute(gemm_mxfp8_ws_kernel<OUT, DEBUG>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxfp8_ws_kernel<OUT, DEBUG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kMxSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_mxfp8_pair_ws_kernel<OUT, DEBUG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kMxSmemBytes));
+                              static_cast<int>(kMxPairSmemBytes));
 }
 
 }  // namespace
@@ -144,10 +160,13 @@ cudaError_t prepare_gemm_kernels(int* max_pairs) {
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0;
+  int clusters = 0, mx_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_ws_kernel<1, false>, &cfg);
   if (e != cudaSuccess) return e;
-  *max_pairs = clusters;
+  cfg.dynamicSmemBytes = kMxPairSmemBytes;
+  e = cudaOccupancyMaxActiveClusters(&mx_clusters, gemm_mxfp8_pair_ws_kernel<1, false>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pairs = clusters < mx_clusters ? clusters : mx_clusters;
   return cudaSuccess;
 }
 
@@ -162,7 +181,13 @@ cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
   return debug ? launch_one<1, true>(l, stream) : launch_one<1, false>(l, stream);
 }
 
-cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream) {
+cudaError_t launch_mxfp8(int out_dtype, bool debug, int variant, const MxLaunch& l,
+                         cudaStream_t stream) {
+  if (variant == kVariantPair) {
+    if (out_dtype == 0)
+      return debug ? launch_mx_pair<0, true>(l, stream) : launch_mx_pair<0, false>(l, stream);
+    return debug ? launch_mx_pair<1, true>(l, stream) : launch_mx_pair<1, false>(l, stream);
+  }
   if (out_dtype == 0) return debug ? launch_mx<0, true>(l, stream) : launch_mx<0, false>(l, stream);
   return debug ? launch_mx<1, true>(l, stream) : launch_mx<1, false>(l, stream);
 }

@@ -26,6 +26,7 @@ struct GemmLaunch {
 // the block-scaled MXFP8 GEMM (one CTA per 128 x 256 tile, the single variant's schedule)
 struct MxLaunch {
   CUtensorMap tmA, tmB, tmC;
+  CUtensorMap tmSFA, tmSFB;   // pair variant: the packed scales as rows of 128 words
   const void* SFA;   // packed scale atoms (mx_pack_scales_kernel)
   const void* SFB;
   uint32_t sfa_blocks, sfb_blocks;   // row blocks of 128 per k-block in the packed arrays
@@ -43,14 +44,16 @@ struct MxLaunch {
 enum Variant { kVariantSingle = 1, kVariantPair = 2 };
 
 // Sets the dynamic shared-memory limit of every GEMM instantiation on the current device and
-// returns how many CTA pairs of the pair kernel can be resident at once (*max_pairs).
+// returns how many CTA pairs of the pair kernels can be resident at once (*max_pairs: the
+// smaller of the dense and the MXFP8 pair kernel).
 cudaError_t prepare_gemm_kernels(int* max_pairs);
 // dtype 0 = fp16, 1 = bf16.  For the pair variant l.grid counts CTAs (even) and l.m_blocks
 // counts 256-row pair tiles.
 cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
                         cudaStream_t stream);
-// out_dtype 0 = fp16, 1 = bf16
-cudaError_t launch_mxfp8(int out_dtype, bool debug, const MxLaunch& l, cudaStream_t stream);
+// out_dtype 0 = fp16, 1 = bf16; variant kVariantSingle or kVariantPair (l.grid counts CTAs)
+cudaError_t launch_mxfp8(int out_dtype, bool debug, int variant, const MxLaunch& l,
+                         cudaStream_t stream);
 // row-major scales [rows, 4 * k_blocks] -> atoms [k_blocks][row_blocks][512]
 cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_blocks,
                            uint32_t row_blocks, cudaStream_t stream);

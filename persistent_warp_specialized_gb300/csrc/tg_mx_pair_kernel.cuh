@@ -1,0 +1,287 @@
+// tg_mx_pair_kernel.cuh -- the CTA-pair (tcgen05 cta_group::2) block-scaled MXFP8 GEMM.
+//
+// The page's MXFP8 example runs on CTA pairs ("[Feature] Introduce tile scheduler #2441",
+// examples/blockscaled_gemm_sm100/gemm_mxfp8_blockscaled_1d1d.py, ``cluster_size = 2``, and
+// the review comments on its ``bx = m_idx * cluster_size + cta_id``).  A cluster of two CTAs
+// shares one 256 x 256 output tile of the product defined in tg_mx_kernel.cuh; the scheduler
+// runs per pair over ceil(M / 256) x ceil(N / 256) tiles (with the tail split into 128-wide
+// half units), as in tg_gemm_pair_kernel.cuh.
+//
+// Per CTA r and stage j of the unit (phase p = w * stages + j, slot s = p % S), for each of the
+// stage's k-blocks k:
+//   * producer (lane 0 of warp 0, both CTAs): wait its own consumed[s]; the even CTA arms its
+//     loaded[s] with both CTAs' bytes; TMA-load A rows 256 m + 128 r (128 x 128 bytes), B rows
+//     n0 + 128 r (n0 + 64 r in a half unit; 128 rows, of which the MMA reads the first 64 then),
+//     the SFA atom of row block 2m + r and the two SFB atoms of the unit's first row block, all
+//     with .cta_group::2 so the bytes complete on the even CTA's loaded[s];
+//   * MMA (lane 0 of warp 1, even CTA): wait loaded[s]; tcgen05.cp .cta_group::2 copies each
+//     CTA's three atoms of slot s into its own TMEM scale slot s; four tcgen05.mma cta_group::2
+//     kind::mxf8f6f4.block_scale 256 x N x 32 into each CTA's 128 rows of the accumulator;
+//     commit with CTA mask 0b11 to consumed[s] (both CTAs); after the k-loop to tmem_full;
+//   * epilogue (warps 4..7, both CTAs): as in tg_mx_kernel.cuh for the CTA's 128 rows; the
+//     release of the accumulator arrives on the even CTA's tmem_empty (count 256).
+// Bounded waits, abort propagation to the peer and the closing cluster barrier are those of
+// tg_gemm_pair_kernel.cuh.
+//
+// Shared memory (1024-byte aligned): S stages of KB k-blocks (KB x 16 KiB of A, then KB x 16
+// KiB of B, K-major, 128-byte swizzle), S x KB atom sets of 1536 bytes, one 4 KiB epilogue
+// buffer per epilogue warp.
+#pragma once
+
+#include "tg_gemm_pair_kernel.cuh"
+#include "tg_mx_kernel.cuh"
+
+namespace tg {
+
+struct __align__(8) MxPairCtl {
+  uint64_t loaded[kMxPairStages];    // used in the even CTA only
+  uint64_t consumed[kMxPairStages];
+  uint64_t tmem_full;
+  uint64_t tmem_empty;               // used in the even CTA only (count 256)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// OUT: 0 = fp16 output, 1 = bf16 output.  p.m_blocks counts 256-row pair tiles.
+template <int OUT, bool DEBUG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_mxfp8_pair_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB,
+                              const __grid_constant__ CUtensorMap tmC,
+                              const __grid_constant__ CUtensorMap tmSFA,
+                              const __grid_constant__ CUtensorMap tmSFB, const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ MxPairCtl ctl;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = cluster_ctarank();          // 0: even CTA (issues the MMA), 1: odd
+  const uint32_t pair = blockIdx.x >> 1;
+  const uint32_t num_pairs = gridDim.x >> 1;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  // stage s: A k-blocks g at sA0 + s * kMxPairStageBytes + g * kMxABytes, then B k-blocks at
+  // sB0 + s * kMxPairStageBytes + g * kMxPairBBytes; atom set (s, g) at sAtom0 + (s * KB + g) * 1536
+  const uint32_t sA0 = sbase;
+  const uint32_t sB0 = sbase + kMxPairKB * kMxABytes;
+  const uint32_t sAtom0 = sbase + kMxPairStages * kMxPairStageBytes;
+  const uint32_t sEpi = sAtom0 + kMxPairAtomRegionBytes;
+
+  const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
+  const uint32_t bar_consumed = smem_u32(&ctl.consumed[0]);
+  const uint32_t bar_tmem_full = smem_u32(&ctl.tmem_full);
+  const uint32_t bar_tmem_empty = smem_u32(&ctl.tmem_empty);
+  const uint32_t bar_drain = smem_u32(&ctl.drain);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kMxPairStages; ++s) {
+      mbar_init(bar_loaded + 8u * s, 1);
+      mbar_init(bar_consumed + 8u * s, 1);
+    }
+    mbar_init(bar_tmem_full, 1);
+    mbar_init(bar_tmem_empty, 2 * kEpiThreads);
+    mbar_init(bar_drain, 1);
+    ctl.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+    prefetch_tensormap(&tmSFA);
+    prefetch_tensormap(&tmSFB);
+  }
+  __syncwarp();
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tcgen05_fence_before_sync();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrive or complete_tx
+  tcgen05_fence_after_sync();
+
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&ctl.abort), rank ^ 1u);
+  const uint64_t limit = p.watchdog_ns;
+  const uint64_t k_stages = (p.k_blocks + kMxPairKB - 1) / kMxPairKB;   // stages per unit
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units, p.column_major);
+      sched.init(pair);
+      uint32_t pending = 0, pending_par = 0;
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint64_t w = sched.current_iter;
+        const bool half = sched.part >= 0;
+        const int32_t m0 = static_cast<int32_t>(sched.m_idx * (2 * kBM) + rank * kBM);
+        const int32_t nu = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
+        const int32_t nr = nu + static_cast<int32_t>(rank) * (half ? kBN / 4 : kBN / 2);
+        const int32_t sfa_row = static_cast<int32_t>(sched.m_idx * 2 + rank);   // row block of A
+        const int32_t sfb_row = nu / kBM;                                      // first row block of B
+        for (uint32_t j = 0; j < k_stages; ++j) {
+          const uint64_t phase = w * k_stages + j;
+          const uint32_t s = static_cast<uint32_t>(phase % kMxPairStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kMxPairStages) & 1u);
+          if (!pair_wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, peer_abort, limit,
+                                  kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          pending &= ~(1u << s);
+          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
+          if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, kMxPairTxBytes);
+#pragma unroll
+          for (uint32_t g = 0; g < kMxPairKB; ++g) {
+            // k-blocks past K read as zeros (TMA fill past the tensor's edge)
+            const uint32_t k = j * kMxPairKB + g;
+            const int32_t kx = static_cast<int32_t>(k * kMxBK);
+            const uint32_t atom = sAtom0 + (s * kMxPairKB + g) * kMxAtomSetBytes;
+            tma_load_2d_pair(sA0 + s * kMxPairStageBytes + g * kMxABytes, &tmA, full_even, kx, m0);
+            tma_load_2d_pair(sB0 + s * kMxPairStageBytes + g * kMxPairBBytes, &tmB, full_even, kx, nr);
+            tma_load_2d_pair(atom, &tmSFA, full_even, 0,
+                             static_cast<int32_t>(k * p.sfa_blocks) + sfa_row);
+            tma_load_2d_pair(atom + kMxSfAtomBytes, &tmSFB, full_even, 0,
+                             static_cast<int32_t>(k * p.sfb_blocks) + sfb_row);
+          }
+          pending |= 1u << s;
+          pending_par = (pending_par & ~(1u << s)) | (par << s);
+        }
+        sched.next_tile();
+      }
+      if (!ok) {
+        if (rank == 0) {
+          for (uint32_t s = 0; s < kMxPairStages; ++s)
+            if ((pending >> s) & 1u)
+              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+        } else if (pending) {
+          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
+          // give them time to land before this CTA may leave
+          spin_ns(limit < 1000000ull ? limit : 1000000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units, p.column_major);
+      sched.init(pair);
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint32_t w = sched.current_iter;
+        if (!pair_wait_or_abort(bar_tmem_empty, (w & 1u) ^ 1u, abort_flag, peer_abort, limit,
+                                kRoleMma)) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after_sync();
+        const uint32_t idesc = sched.part >= 0 ? idesc_mxf8(2 * kBM, kBN / 2, 0, 0)
+                                               : idesc_mxf8(2 * kBM, kBN, 0, 0);
+        for (uint32_t j = 0; j < k_stages; ++j) {
+          const uint64_t phase = static_cast<uint64_t>(w) * k_stages + j;
+          const uint32_t s = static_cast<uint32_t>(phase % kMxPairStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kMxPairStages) & 1u);
+          if (!pair_wait_or_abort(bar_loaded + 8u * s, par, abort_flag, peer_abort, limit,
+                                  kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after_sync();
+#pragma unroll
+          for (uint32_t g = 0; g < kMxPairKB; ++g) {
+            const uint32_t k = j * kMxPairKB + g;
+            if (k >= p.k_blocks) break;   // the zero-filled tail of the last stage
+            const uint32_t atom = sAtom0 + (s * kMxPairKB + g) * kMxAtomSetBytes;
+            const uint32_t t_sf = tmem_base + kMxAccCols + (s * kMxPairKB + g) * kMxSfColsPerStage;
+            tmem_cp_32x128b_x4_pair(t_sf, smem_desc_plain(atom, 128, 128));
+            tmem_cp_32x128b_x4_pair(t_sf + 4, smem_desc_plain(atom + kMxSfAtomBytes, 128, 128));
+            tmem_cp_32x128b_x4_pair(t_sf + 8, smem_desc_plain(atom + 2 * kMxSfAtomBytes, 128, 128));
+            const uint32_t a_addr = sA0 + s * kMxPairStageBytes + g * kMxABytes;
+            const uint32_t b_addr = sB0 + s * kMxPairStageBytes + g * kMxPairBBytes;
+#pragma unroll
+            for (uint32_t kk = 0; kk < kMxBK / kMxUmmaK; ++kk) {
+              const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kMxUmmaK, 16, 1024);
+              const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kMxUmmaK, 16, 1024);
+              umma_mxf8_pair(tmem_base, a_desc, b_desc, idesc | (kk << 29) | (kk << 4), t_sf,
+                             t_sf + 4, (k | kk) != 0u ? 1u : 0u);
+            }
+          }
+          umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(bar_tmem_full, 0x3);
+        sched.next_tile();
+      }
+      umma_commit_pair_multicast(bar_drain, 0x1);
+      wait_bounded(bar_drain, 0, limit, kRoleDrain);
+    }
+    __syncwarp();
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const uint32_t q = warp - kFirstEpiWarp;       // TMEM lanes 32q .. 32q + 31
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                  p.total_units, p.column_major);
+    sched.init(pair);
+    const uint32_t sbuf = sEpi + q * kEpiBufBytes;
+    const uint32_t empty_even = mapa_shared(bar_tmem_empty, 0);
+    while (sched.valid()) {
+      const uint32_t w = sched.current_iter;
+      const bool got = pair_wait_or_abort(bar_tmem_full, w & 1u, abort_flag, peer_abort, limit,
+                                          kRoleEpilogue);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tcgen05_fence_after_sync();
+      const bool half = sched.part >= 0;
+      const int32_t row0 = static_cast<int32_t>(sched.m_idx * (2 * kBM) + rank * kBM + q * 32u);
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16);
+      uint32_t packed[kBN / kEpiN][kEpiN / 2];
+#pragma unroll
+      for (uint32_t j = 0; j < kBN / kEpiN; ++j) {
+        if (half && j >= kBN / kEpiN / 2) break;
+#pragma unroll
+        for (uint32_t h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row + j * kEpiN + h * 32u, v);
+#pragma unroll
+          for (uint32_t c = 0; c < 16; ++c) packed[j][16 * h + c] = pack_out<OUT>(v[2 * c], v[2 * c + 1]);
+        }
+      }
+      tcgen05_fence_before_sync();
+      mbar_arrive_cluster(empty_even);   // accumulator in registers: the next tile may start
+#pragma unroll
+      for (uint32_t j = 0; j < kBN / kEpiN; ++j) {
+        if (half && j >= kBN / kEpiN / 2) break;
+        mx_store_chunk(packed[j], lane, sbuf, &tmC, p.M, p.N, row0,
+                       col0 + static_cast<int32_t>(j * kEpiN));
+      }
+      if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
+        int32_t* tr = p.trace + 5ull * sched.linear_idx;
+        tr[0] = static_cast<int32_t>(pair);
+        tr[1] = static_cast<int32_t>(w);
+        tr[2] = static_cast<int32_t>(sched.m_idx);
+        tr[3] = static_cast<int32_t>(sched.n_idx);
+        tr[4] = sched.part;
+      }
+      sched.next_tile();
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tcgen05_fence_before_sync();
+  cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
+  if (warp == 2) {
+    tcgen05_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tg

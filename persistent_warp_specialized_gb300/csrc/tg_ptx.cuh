@@ -251,6 +251,28 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
                : "memory");
 }
 
+// The pair form: issued by the even CTA, copies each CTA's atom at ``sdesc`` into that CTA's
+// own TMEM at ``taddr`` (measured on GB300), replicated into its four lane quadrants.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * 2^SFA) . (B * 2^SFB) over the CTA pair (M = 256): A rows and B columns as
+// umma_f16_pair; each CTA's scales come from its own TMEM (A rows 128r.. from CTA r; all of B's
+// columns in both).  Issued by one thread of the even CTA.
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= (A * 2^SFA) . (B * 2^SFB): E4M3 operands from shared memory, E8M0 scales from
 // TMEM (one per 32 K-elements, byte ids in the instruction descriptor).  One thread issues it.
 __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,

@@ -33,15 +33,20 @@ def device_inputs(a, sa, b, sb):
     return a.cuda(), tg.mxfp8_pack(sa.cuda(), K), b.cuda(), tg.mxfp8_pack(sb.cuda(), K)
 
 
-def run_mx(a, sa, b, sb, out="bf16", debug=False, **kw):
+MX_VARIANTS = ["single", "pair"]
+
+
+def run_mx(a, sa, b, sb, out="bf16", debug=False, variant="auto", **kw):
     M, K = a.shape
     N = b.shape[0]
     c = nan_filled(M, N, out)
     dev = device_inputs(a, sa, b, sb)
     if debug:
-        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, out, **kw)
-    else:
+        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, out, variant=variant, **kw)
+    elif variant == "auto":
         tg.tg_gemm_mxfp8(*dev, c, M, N, K, out)
+    else:
+        tg.tg_gemm_mxfp8_ex(*dev, c, M, N, K, out, variant=variant)
     torch.cuda.synchronize()
     assert tg.tg_device_status() == 0
     return wl.bits(c.cpu())
@@ -94,23 +99,27 @@ def test_pack_scales_is_the_documented_layout(rows, K):
     assert np.array_equal(packed.cpu().numpy(), packed_layout(sf.numpy(), K))
 
 
+@pytest.mark.parametrize("variant", MX_VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (512, 768, 512), (1000, 520, 384),
-                                   (4096, 4096, 128), (2560, 2560, 256), (8, 8, 128)])
-def test_integer_inputs_are_bit_exact(M, N, K):
+                                   (4096, 4096, 128), (2560, 2560, 256), (8, 8, 128),
+                                   (384, 640, 256)])
+def test_integer_inputs_are_bit_exact(M, N, K, variant):
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=M + N + K)
-    assert np.array_equal(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb))
+    assert np.array_equal(run_mx(a, sa, b, sb, variant=variant), ref_bits(a, sa, b, sb))
 
 
+@pytest.mark.parametrize("variant", MX_VARIANTS)
 @pytest.mark.parametrize("out", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1024, 1024, 1024), (1000, 520, 2048),
                                    (4000, 7000, 2048)])
-def test_quantized_normal_inputs_within_tolerance(M, N, K, out):
+def test_quantized_normal_inputs_within_tolerance(M, N, K, out, variant):
     a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed=7 * M + K)
-    check_tolerance(run_mx(a, sa, b, sb, out), ref_bits(a, sa, b, sb, out), a, sa, b, sb, out,
-                    f"{M}x{N}x{K} {out}")
+    check_tolerance(run_mx(a, sa, b, sb, out, variant=variant), ref_bits(a, sa, b, sb, out), a, sa,
+                    b, sb, out, f"{M}x{N}x{K} {out} {variant}")
 
 
-def test_scales_span_the_e8m0_range():
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_scales_span_the_e8m0_range(variant):
     # element blocks scaled from 2^-60 to 2^+60 (all products stay normal in fp32).  Here an
     # output can be the small residue of block terms 10^7 .. 10^13 times larger that cancel,
     # and no fp32 accumulation order meets the relative gate there (an in-order fp32 sum of
@@ -121,18 +130,21 @@ def test_scales_span_the_e8m0_range():
     gen = torch.Generator().manual_seed(11)
     sa = torch.randint(127 - 30, 127 + 31, (M, K // 32), generator=gen).to(torch.uint8)
     sb = torch.randint(127 - 30, 127 + 31, (N, K // 32), generator=gen).to(torch.uint8)
-    check_tolerance(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb), a, sa, b, sb, "bf16", "scales",
-                    gate=False)
+    check_tolerance(run_mx(a, sa, b, sb, variant=variant), ref_bits(a, sa, b, sb), a, sa, b, sb,
+                    "bf16", "scales", gate=False)
 
 
+@pytest.mark.parametrize("variant", MX_VARIANTS)
 @pytest.mark.parametrize("plain,column_major", [(False, False), (True, False), (False, True)])
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4000, 7000, 128), (256, 256, 256)])
-def test_kernel_followed_the_schedule(M, N, K, plain, column_major):
-    shape = tg.tg_gemm_launch_shape(M, N, K, "single", plain)
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4000, 7000, 128), (256, 256, 256),
+                                   (8192, 8192, 128)])
+def test_kernel_followed_the_schedule(M, N, K, plain, column_major, variant):
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
     units = shape["units"]
     trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=5)
-    got_c = run_mx(a, sa, b, sb, debug=True, trace=trace, plain=plain, column_major=column_major)
+    got_c = run_mx(a, sa, b, sb, debug=True, variant=variant, trace=trace, plain=plain,
+                   column_major=column_major)
     want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"],
                                     tg.tg_gemm_config()["group"], split_tail=not plain,
                                     column_major=column_major)
@@ -145,17 +157,19 @@ def test_kernel_followed_the_schedule(M, N, K, plain, column_major):
     assert np.array_equal(got_c, ref_bits(a, sa, b, sb))
 
 
-def test_watchdog_fires_and_context_survives():
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_watchdog_fires_and_context_survives(variant):
     M, N, K = 512, 512, 1024
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=1)
     dev = device_inputs(a, sa, b, sb)
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tg.TgError) as e:
-        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, "bf16", watchdog_ns=20_000_000,
-                               inject_skip_phase=5)
+        # phase 2 exists in both kernels (single: k-blocks 0..7; pair: stages of 2 k-blocks)
+        tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, "bf16", variant=variant, watchdog_ns=20_000_000,
+                               inject_skip_phase=2)
     assert e.value.code == tg.TG_ERR_TIMEOUT
     assert tg.tg_device_status() == 0
-    assert np.array_equal(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb))
+    assert np.array_equal(run_mx(a, sa, b, sb, variant=variant), ref_bits(a, sa, b, sb))
 
 
 def test_empty_and_zero_k():
@@ -167,10 +181,11 @@ def test_empty_and_zero_k():
     assert tg.tg_gemm_mxfp8(None, None, None, None, None, 0, 64, 128, "bf16") == 0
 
 
-def test_full_size_workload_sampled_entries():
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_full_size_workload_sampled_entries(variant):
     M, N, K, seed = wl.MX_WORKLOADS["mxfp8_8192"]
     a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed)
-    c = run_mx(a, sa, b, sb)
+    c = run_mx(a, sa, b, sb, variant=variant)
     rng = np.random.default_rng(0)
     rows = np.concatenate([[0, M - 1], rng.choice(M, 62, replace=False)])
     cols = np.concatenate([[0, N - 1], rng.choice(N, 62, replace=False)])
