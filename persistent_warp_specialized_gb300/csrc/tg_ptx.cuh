@@ -1,5 +1,7 @@
-// tg_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// and the 5th-generation tensor core (tcgen05: TMEM alloc, mma, commit, ld).
+// tg_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor) and
+// bulk copies, the 5th-generation tensor core (tcgen05: TMEM alloc, mma -- kind::f16 and the
+// block-scaled kind::mxf8f6f4 --, cp, commit, ld), clusters and CTA pairs (cta_group::2),
+// and cluster launch control.
 //
 // These are the primitives the warp roles of "[Feature] Introduce tile scheduler #2441"
 // (gemm_tcgen5mma_ws_persistent.py) name as DSL calls: T.mbarrier_wait_parity,
