@@ -96,6 +96,7 @@ def bits(t):
 MX_WORKLOADS = {
     "mxfp8_8192": (8192, 8192, 8192, 6),   # M, N, K, seed
     "mxfp8_6144": (6144, 6144, 6144, 8),   # a smaller case for detailed profiles
+    "mxfp8_512": (512, 512, 512, 9),       # a small case the oracle finishes at once
 }
 MX_BLOCK = 32
 

@@ -98,3 +98,16 @@ def test_reference_arm_nonzero_rank_does_no_work():
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_mxfp8_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "mxfp8_512", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["config"]["workload"] == "mxfp8_512" and d["config"]["in_dtype"] == "e4m3"
+    assert d["cpu_baseline"]["kind"] == "oracle"
