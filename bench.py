@@ -11,7 +11,8 @@ over K back-to-back steps after W warm-up steps.  The 8192^3 bf16 inputs (A + B 
 are larger than the 129 MB L2, so no flush runs between steps.
 
 Also reported: ``e2e`` (the same metric through tg_gemm_persistent_host: pinned host A, B
-copied in and C copied out every step), ``roofline`` (tensor-bound: achieved TFLOP/s over
+copied in and C copied out every step; consecutive steps alternate between two streams with
+their own device buffers, so one step's copies overlap the other's GEMM), ``roofline`` (tensor-bound: achieved TFLOP/s over
 the measured cuBLAS bf16 peak of this GPU type), ``clocks`` (nvidia-smi sampled during the
 timed region) and ``cpu_baseline`` (the CPU oracle timed on a bounded row slab of the same
 workload, which also checks the GPU's rows of that slab).
@@ -318,6 +319,35 @@ def timed_region(step, steps, warm, dev, stream, world):
     return ms_local, max_over_ranks(ms_local, dev if world > 1 else None), clocks
 
 
+def time_e2e(make_step, e_steps, dev, world, lanes=2):
+    """ms per step of end-to-end steps issued round-robin on ``lanes`` streams, each with its
+    own buffers (make_step(j, stream) -> step function), so one step's copies overlap another's
+    kernels.  Every step copies its own inputs in and its result out."""
+    import torch
+
+    streams = [torch.cuda.Stream(dev) for _ in range(lanes)]
+    steps = [make_step(j, streams[j]) for j in range(lanes)]
+    for i in range(2 * lanes):
+        steps[i % lanes]()
+    torch.cuda.synchronize(dev)
+    barrier()
+    cur = torch.cuda.current_stream(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(cur)
+    for st in streams:
+        st.wait_event(start)
+    for i in range(e_steps):
+        steps[i % lanes]()
+    for st in streams:
+        done = torch.cuda.Event()
+        done.record(st)
+        cur.wait_event(done)
+    end.record(cur)
+    torch.cuda.synchronize(dev)
+    return max_over_ranks(start.elapsed_time(end) / e_steps, dev if world > 1 else None)
+
+
 def run_tg(args):
     import torch
 
@@ -353,33 +383,25 @@ def run_tg(args):
     steps, warm = max(1, args.steps), max(3, args.warmup)
     ms_local, ms, clocks = timed_region(step, steps, warm, dev, stream, world)
     value = world * w.flops / (ms * 1e-3) / 1e12
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
 
     # end to end through the host-buffer entry point: H2D A, B + kernel + D2H C per step
     a_h, b_h = a_cpu.pin_memory(), b_cpu.pin_memory()
-    c_h = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.dtype]).pin_memory()
-    a2, b2, c2 = torch.empty_like(a), torch.empty_like(b), torch.empty_like(c)
 
-    def e2e_step():
-        tg.tg_gemm_persistent_host(a_h, b_h, c_h, a2, b2, c2, w.M, w.N, w.K, w.dtype, stream)
+    def make_e2e_step(j, st):
+        c_h = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.dtype]).pin_memory()
+        a2, b2, c2 = torch.empty_like(a), torch.empty_like(b), torch.empty_like(c)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e_steps = max(1, args.e2e_steps)
-    barrier()
-    ev0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e_steps, dev if world > 1 else None)
+        def e2e_step():
+            tg.tg_gemm_persistent_host(a_h, b_h, c_h, a2, b2, c2, w.M, w.N, w.K, w.dtype, st)
+        return e2e_step
+
+    e_ms = time_e2e(make_e2e_step, max(1, args.e2e_steps), dev, world)
     tg.tg_device_status(stream)
     h2d = 2 * (w.M * w.K + w.K * w.N)
     d2h = 2 * w.M * w.N
     e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+           "streams": 2, "api": "tg_gemm_persistent_host"}
 
     launch = tg.tg_gemm_launch_shape(w.M, w.N, w.K, args.variant)
     kernel = KERNEL_NAMES[launch["variant"]]
@@ -542,35 +564,28 @@ def run_tg_mx(args):
 
     # end to end: pinned host inputs copied in, scales packed, the GEMM, C copied out
     pinned = [t.pin_memory() for t in host]
-    dev2 = [torch.empty_like(t, device=dev) for t in host]
-    c2 = torch.empty_like(c)
-    c_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step():
-        for d, h in zip(dev2, pinned):
-            d.copy_(h, non_blocking=True)
-        tg.tg_mxfp8_pack_scales(dev2[1], sa_p, M, K, stream)
-        tg.tg_mxfp8_pack_scales(dev2[3], sb_p, N, K, stream)
-        tg.tg_gemm_mxfp8(dev2[0], sa_p, dev2[2], sb_p, c2, M, N, K, "bf16", stream)
-        c_h.copy_(c2, non_blocking=True)
+    def make_e2e_step(j, st):
+        dev2 = [torch.empty_like(t, device=dev) for t in host]
+        sa2, sb2, c2 = torch.empty_like(sa_p), torch.empty_like(sb_p), torch.empty_like(c)
+        c_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    e_steps = max(1, args.e2e_steps)
-    barrier()
-    ev0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e_steps, dev if world > 1 else None)
+        def e2e_step():
+            with torch.cuda.stream(st):
+                for d, h in zip(dev2, pinned):
+                    d.copy_(h, non_blocking=True)
+            tg.tg_mxfp8_pack_scales(dev2[1], sa2, M, K, st)
+            tg.tg_mxfp8_pack_scales(dev2[3], sb2, N, K, st)
+            tg.tg_gemm_mxfp8(dev2[0], sa2, dev2[2], sb2, c2, M, N, K, "bf16", st)
+            with torch.cuda.stream(st):
+                c_h.copy_(c2, non_blocking=True)
+        return e2e_step
+
+    e_ms = time_e2e(make_e2e_step, max(1, args.e2e_steps), dev, world)
     tg.tg_device_status(stream)
     e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": sum(t.numel() for t in host), "d2h_bytes_per_step": 2 * M * N,
-           "ms_per_step": e_ms}
+           "ms_per_step": e_ms, "streams": 2}
 
     peaks, peak_src = measured_peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12    # the GEMM kernel alone
