@@ -546,15 +546,15 @@ def run_tg_mx(args):
     flops = 2.0 * M * N * K
 
     # a step: both operands' row-major scales packed, then the GEMM (three launches)
+    def gemm_only():
+        tg.tg_gemm_mxfp8_ex(a, sa_p, b, sb_p, c, M, N, K, "bf16", stream, args.variant)
+
     def step():
         tg.tg_mxfp8_pack_scales(sa, sa_p, M, K, stream)
         tg.tg_mxfp8_pack_scales(sb, sb_p, N, K, stream)
-        tg.tg_gemm_mxfp8(a, sa_p, b, sb_p, c, M, N, K, "bf16", stream)
+        gemm_only()
 
-    def gemm_only():
-        tg.tg_gemm_mxfp8(a, sa_p, b, sb_p, c, M, N, K, "bf16", stream)
-
-    launch = tg.tg_gemm_launch_shape(M, N, K, "auto")   # tg_gemm_mxfp8 chooses as this does
+    launch = tg.tg_gemm_launch_shape(M, N, K, args.variant)   # the GEMM's kernel and launch
     kernel = "gemm_mxfp8_pair_ws" if launch["variant"] == tg.TG_VARIANT_PAIR else "gemm_mxfp8_ws"
 
     steps, warm = max(1, args.steps), max(3, args.warmup)
@@ -576,7 +576,7 @@ def run_tg_mx(args):
                     d.copy_(h, non_blocking=True)
             tg.tg_mxfp8_pack_scales(dev2[1], sa2, M, K, st)
             tg.tg_mxfp8_pack_scales(dev2[3], sb2, N, K, st)
-            tg.tg_gemm_mxfp8(dev2[0], sa2, dev2[2], sb2, c2, M, N, K, "bf16", st)
+            tg.tg_gemm_mxfp8_ex(dev2[0], sa2, dev2[2], sb2, c2, M, N, K, "bf16", st, args.variant)
             with torch.cuda.stream(st):
                 c_h.copy_(c2, non_blocking=True)
         return e2e_step
