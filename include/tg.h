@@ -63,6 +63,10 @@ enum {
   TG_SCHEDULE_SPLIT_TAIL = 0x1
 };
 
+/* OR'ed into a variant: the group width of the grouped tile order (the scheduler's
+   swizzle_size), 1..255; 0 (not given) = 8, the page's group_size. */
+#define TG_SCHEDULE_GROUP(g) (((int)(g) & 0xFF) << 16)
+
 /* status codes */
 enum {
   TG_OK = 0,

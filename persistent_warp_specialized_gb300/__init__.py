@@ -150,30 +150,39 @@ def tg_gemm_persistent(A, B, C, M, N, K, dtype, stream=None):
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream)))
 
 
-def _variant(v, plain=False, column_major=False, dynamic=False):
+def _group(g):
+    """TG_SCHEDULE_GROUP(g): the grouped order's width (None: the library's default, 8)."""
+    if g is None:
+        return 0
+    if not 1 <= int(g) <= 255:
+        raise ValueError(f"group width {g} outside 1..255")
+    return int(g) << 16
+
+
+def _variant(v, plain=False, column_major=False, dynamic=False, group=None):
     """"auto" / "single" / "pair" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
     return (code | (TG_SCHEDULE_PLAIN if plain else 0)
             | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
-            | (TG_SCHEDULE_DYNAMIC if dynamic else 0))
+            | (TG_SCHEDULE_DYNAMIC if dynamic else 0) | _group(group))
 
 
 def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
-                          column_major=False, dynamic=False):
+                          column_major=False, dynamic=False, group=None):
     """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
     ``plain`` walks the page's tile order with no tail split; ``column_major`` the scheduler's
     column-major order."""
     return _check(load_library().tg_gemm_persistent_ex(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major, dynamic)))
+        _variant(variant, plain, column_major, dynamic, group)))
 
 
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
                              watchdog_ns=0, inject_skip_phase=-1, plain=False,
-                             column_major=False, dynamic=False):
+                             column_major=False, dynamic=False, group=None):
     return _check(load_library().tg_gemm_persistent_debug(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major, dynamic), _ptr(trace), watchdog_ns,
+        _variant(variant, plain, column_major, dynamic, group), _ptr(trace), watchdog_ns,
         inject_skip_phase))
 
 
@@ -223,9 +232,8 @@ def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True, col
     return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
 
 
-def _mx_flags(variant="auto", plain=False, column_major=False):
-    return (VARIANTS[variant] | (TG_SCHEDULE_PLAIN if plain else 0)
-            | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0))
+def _mx_flags(variant="auto", plain=False, column_major=False, group=None):
+    return _variant(variant, plain, column_major, False, group)
 
 
 def tg_mxfp8_scale_bytes(rows, K):
@@ -256,18 +264,18 @@ def tg_gemm_mxfp8(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None):
 
 
 def tg_gemm_mxfp8_ex(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None, variant="auto",
-                     plain=False, column_major=False):
+                     plain=False, column_major=False, group=None):
     return _check(load_library().tg_gemm_mxfp8_ex(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
-        _stream(stream), _mx_flags(variant, plain, column_major)))
+        _stream(stream), _mx_flags(variant, plain, column_major, group)))
 
 
 def tg_gemm_mxfp8_debug(A, SFA, B, SFB, C, M, N, K, out_dtype="bf16", stream=None, trace=None,
                         watchdog_ns=0, inject_skip_phase=-1, variant="auto", plain=False,
-                        column_major=False):
+                        column_major=False, group=None):
     return _check(load_library().tg_gemm_mxfp8_debug(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _dtype(out_dtype),
-        _stream(stream), _mx_flags(variant, plain, column_major), _ptr(trace), watchdog_ns,
+        _stream(stream), _mx_flags(variant, plain, column_major, group), _ptr(trace), watchdog_ns,
         inject_skip_phase))
 
 

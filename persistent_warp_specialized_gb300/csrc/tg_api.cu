@@ -216,11 +216,19 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
   return sh;
 }
 
-constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | TG_SCHEDULE_DYNAMIC;
+constexpr int kGroupBits = TG_SCHEDULE_GROUP(0xFF);
+constexpr int kScheduleFlags =
+    TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | TG_SCHEDULE_DYNAMIC | kGroupBits;
 
 bool known_variant(int v) {
   const int kernel = v & ~kScheduleFlags;
   return kernel == TG_VARIANT_AUTO || kernel == TG_VARIANT_SINGLE || kernel == TG_VARIANT_PAIR;
+}
+
+// The group width a variant asks for (TG_SCHEDULE_GROUP), or the default.
+uint32_t group_of(int v) {
+  const uint32_t g = (static_cast<uint32_t>(v) & static_cast<uint32_t>(kGroupBits)) >> 16;
+  return g ? g : static_cast<uint32_t>(tg::kGroup);
 }
 
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
@@ -230,6 +238,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   const uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
+  const uint32_t group = group_of(variant);
   variant &= ~kScheduleFlags;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
@@ -263,7 +272,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.column_major = column_major;
   l.dynamic = dynamic ? 1u : 0u;
   l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
-  l.group = tg::kGroup;
+  l.group = group;
   l.grid = sh.ctas;
   l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
   l.trace = trace;
@@ -338,9 +347,10 @@ int validate_mx(const void* A, const void* SFA, const void* B, const void* SFB, 
 int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M,
             int64_t N, int64_t K, int out_dtype, void* stream, int flags, bool debug,
             int32_t* trace, uint64_t watchdog_ns, int64_t inject) {
-  int variant = flags & ~(TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR);
+  int variant = flags & ~(TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | kGroupBits);
   if (variant != TG_VARIANT_AUTO && variant != TG_VARIANT_SINGLE && variant != TG_VARIANT_PAIR)
     return fail(TG_ERR_ARG, "unknown MXFP8 variant or schedule flags 0x%x", flags);
+  const uint32_t group = group_of(flags);
   bool nothing = false;
   int rc = validate_mx(A, SFA, B, SFB, C, M, N, K, out_dtype, &nothing);
   if (rc != TG_OK || nothing) return rc;
@@ -388,7 +398,7 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
   l.m_blocks = sh.m_tiles;
   l.n_blocks = sh.n_tiles;
   l.k_blocks = static_cast<uint32_t>(K / tg::kMxBK);
-  l.group = tg::kGroup;
+  l.group = group;
   l.split_from = sh.split_from;
   l.total_units = sh.units;
   l.column_major = (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;

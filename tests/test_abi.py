@@ -136,3 +136,18 @@ def test_mxfp8_packed_scale_sizes_and_rejections(lib):
         tg.tg_mxfp8_pack_scales(16, 24, 8, 128, stream=0)          # output not 16-byte aligned
     assert e.value.code == tg.TG_ERR_ALIGN
     assert tg.tg_mxfp8_pack_scales(None, None, 0, 0, stream=0) == 0
+
+
+def test_group_width_option_rejections(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    with pytest.raises(ValueError):
+        tg._group(0)
+    with pytest.raises(ValueError):
+        tg._group(256)
+    assert tg._group(12) == 12 << 16
+    # a bit above the group field is not a known variant
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_gemm_persistent_ex(16, 16, 16, 8, 8, 8, "bf16", stream=0, variant=1 << 24)
+    assert e.value.code == tg.TG_ERR_ARG

@@ -194,3 +194,21 @@ def test_full_size_workload_sampled_entries(variant):
     cv, rv = formats.decode(got, "bf16"), formats.decode(want, "bf16")
     assert np.isfinite(cv).all()
     assert (np.abs(cv - rv) <= ATOL + RTOL * np.abs(rv)).all()
+
+
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_group_width_option_followed(variant):
+    M, N, K, group = 4096, 4096, 128, 12
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant)
+    units = shape["units"]
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
+    a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=12)
+    got_c = run_mx(a, sa, b, sb, debug=True, variant=variant, trace=trace, group=group)
+    want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"], group,
+                                    split_tail=True)
+    by_unit = {worker + w * shape["workers"]: (worker, w, bx, by, part)
+               for (worker, w, bx, by, part) in want}
+    got = trace.cpu().numpy()
+    for u in range(units):
+        assert tuple(int(v) for v in got[u]) == by_unit[u], u
+    assert np.array_equal(got_c, ref_bits(a, sa, b, sb))

@@ -179,3 +179,25 @@ def test_dynamic_needs_single_variant():
     with pytest.raises(tg.TgError) as e:
         tg.tg_gemm_persistent_ex(a, a, c, 256, 256, 256, "bf16", variant="pair", dynamic=True)
     assert e.value.code == tg.TG_ERR_ARG
+
+
+@pytest.mark.parametrize("group", [1, 3, 12])
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 64), (4000, 7000, 128)])
+def test_group_width_option_followed(M, N, K, variant, group):
+    # TG_SCHEDULE_GROUP(g): the kernel walks the grouped order of width g, as the oracle does
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant)
+    units = shape["units"]
+    a, b = wl.small_int_inputs(M, N, K, "bf16", seed=group)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
+    assert tg.tg_gemm_persistent_debug(a.cuda(), b.cuda(), c, M, N, K, "bf16", variant=variant,
+                                       trace=trace, group=group) == 0
+    want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"], group,
+                                    split_tail=True)
+    by_unit = {worker + w * shape["workers"]: (worker, w, bx, by, part)
+               for (worker, w, bx, by, part) in want}
+    got = trace.cpu().numpy()
+    for u in range(units):
+        assert tuple(int(v) for v in got[u]) == by_unit[u], u
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
