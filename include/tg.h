@@ -59,6 +59,10 @@ enum {
      units go to whichever SM frees up first.  The unit-to-CTA assignment is then decided at run
      time (the debug trace records it); the set of units and their decode are unchanged. */
   TG_SCHEDULE_DYNAMIC = 0x400,
+  /* OR'ed into a variant of the dense GEMM: the epilogue stores each thread's row of the tile
+     with 16-byte stores straight from registers (the page's direct C_local_cast store) instead
+     of staging it in shared memory for a TMA store (the page's use_tma_store, the default). */
+  TG_EPILOGUE_DIRECT = 0x800,
   /* tg_tile_schedule_ex flag: apply the tail split (the GEMM does unless TG_SCHEDULE_PLAIN) */
   TG_SCHEDULE_SPLIT_TAIL = 0x1
 };
@@ -242,7 +246,8 @@ int tg_gemm_mxfp8_ex(const void* A_dev, const void* SFA_dev, const void* B_dev,
 /*
  * tg_gemm_mxfp8_debug -- tg_gemm_mxfp8_ex, synchronously, with the inspection aids of
  * tg_gemm_persistent_debug (trace of 5 int32 per unit, watchdog limit, injected missing fill).
- *   flags: as tg_gemm_mxfp8_ex's variant.
+ *   flags: as tg_gemm_mxfp8_ex's variant.  (TG_EPILOGUE_DIRECT is a dense-GEMM option:
+ *   TG_ERR_ARG here.)
  */
 int tg_gemm_mxfp8_debug(const void* A_dev, const void* SFA_dev, const void* B_dev,
                         const void* SFB_dev, void* C_dev, int64_t M, int64_t N, int64_t K,

@@ -29,6 +29,7 @@ TG_SCHEDULE_PLAIN = 0x100
 TG_SCHEDULE_COLUMN_MAJOR = 0x200
 TG_SCHEDULE_SPLIT_TAIL = 0x1
 TG_SCHEDULE_DYNAMIC = 0x400
+TG_EPILOGUE_DIRECT = 0x800
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
@@ -159,22 +160,23 @@ def _group(g):
     return int(g) << 16
 
 
-def _variant(v, plain=False, column_major=False, dynamic=False, group=None):
+def _variant(v, plain=False, column_major=False, dynamic=False, group=None, direct=False):
     """"auto" / "single" / "pair" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
     return (code | (TG_SCHEDULE_PLAIN if plain else 0)
             | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
-            | (TG_SCHEDULE_DYNAMIC if dynamic else 0) | _group(group))
+            | (TG_SCHEDULE_DYNAMIC if dynamic else 0) | _group(group)
+            | (TG_EPILOGUE_DIRECT if direct else 0))
 
 
 def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
-                          column_major=False, dynamic=False, group=None):
+                          column_major=False, dynamic=False, group=None, direct=False):
     """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
     ``plain`` walks the page's tile order with no tail split; ``column_major`` the scheduler's
     column-major order."""
     return _check(load_library().tg_gemm_persistent_ex(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major, dynamic, group)))
+        _variant(variant, plain, column_major, dynamic, group, direct)))
 
 
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,

@@ -217,8 +217,8 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
 }
 
 constexpr int kGroupBits = TG_SCHEDULE_GROUP(0xFF);
-constexpr int kScheduleFlags =
-    TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | TG_SCHEDULE_DYNAMIC | kGroupBits;
+constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR |
+                               TG_SCHEDULE_DYNAMIC | TG_EPILOGUE_DIRECT | kGroupBits;
 
 bool known_variant(int v) {
   const int kernel = v & ~kScheduleFlags;
@@ -239,6 +239,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
   const uint32_t group = group_of(variant);
+  const uint32_t epi_direct = (variant & TG_EPILOGUE_DIRECT) ? 1u : 0u;
   variant &= ~kScheduleFlags;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
@@ -271,6 +272,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.total_units = sh.units;
   l.column_major = column_major;
   l.dynamic = dynamic ? 1u : 0u;
+  l.epi_direct = epi_direct;
   l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
   l.group = group;
   l.grid = sh.ctas;

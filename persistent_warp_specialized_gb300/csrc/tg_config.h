@@ -48,16 +48,9 @@ constexpr int kKAtoms = kBK / kKAtom;
 #ifndef TG_B_POLICY
 #define TG_B_POLICY 0
 #endif
-// Epilogue store path: 0 = through shared memory and TMA stores (the page's use_tma_store),
-// 1 = 16-byte stores straight from registers (the page's direct C_local_cast store), which
-// needs no staging buffers and leaves that shared memory to the operand ring.
-#ifndef TG_EPI_DIRECT
-#define TG_EPI_DIRECT 0
-#endif
 constexpr int kStages = TG_STAGES;
 constexpr int kAPolicy = TG_A_POLICY;
 constexpr int kBPolicy = TG_B_POLICY;
-constexpr bool kEpiDirect = TG_EPI_DIRECT != 0;
 constexpr int kEpiN = 64;
 #ifndef TG_GROUP
 #define TG_GROUP 8
@@ -78,7 +71,7 @@ constexpr uint32_t kBChunkCols = 64;                             // one 128-byte
 constexpr uint32_t kBChunkBytes = kBK * kBChunkCols * kElemBytes;  // 8 KiB
 constexpr uint32_t kEpiBufBytes = 32 * kEpiN * kElemBytes;       // 4 KiB: 32 rows x 128 bytes
 constexpr uint32_t kSmemAlignSlack = 1024;
-constexpr uint32_t kEpiSmemBytes = kEpiDirect ? 0u : kEpiWarps * 2 * kEpiBufBytes;
+constexpr uint32_t kEpiSmemBytes = kEpiWarps * 2 * kEpiBufBytes;
 constexpr uint32_t kSmemBytes = kSmemAlignSlack + kStages * kStageBytes + kEpiSmemBytes;
 constexpr uint32_t kTmemCols = 512;
 

@@ -58,6 +58,7 @@ GemmParams params_of(const GemmLaunch& l) {
   p.split_from = l.split_from;
   p.column_major = l.column_major;
   p.dynamic = l.dynamic;
+  p.epi_direct = l.epi_direct;
   p.total_units = l.total_units;
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;

@@ -54,6 +54,7 @@ struct GemmParams {
   uint32_t split_from, total_units;   // tail split of the scheduler (see tg_tile_scheduler.cuh)
   uint32_t column_major;              // scheduler order option
   uint32_t dynamic;                   // 1: units handed out by cluster launch control
+  uint32_t epi_direct;                // 1: the epilogue stores from registers (no TMA store)
   uint64_t watchdog_ns;
   int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
@@ -132,13 +133,13 @@ __device__ __forceinline__ uint32_t pack_out(uint32_t lo_bits, uint32_t hi_bits)
 //    warp fences the writes into the async proxy, and lane 0 issues one TMA store, which
 //    clips at the tensor's edge.  Two buffers per warp alternate; before one is rewritten,
 //    lane 0 waits until the store that read it is done.  One bulk group per chunk.
-//  * direct: each lane stores its row's 128 bytes with 16-byte stores.
+//  * direct (p.epi_direct): each lane stores its row's 128 bytes with 16-byte stores.
 template <int DT>
 __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], uint32_t lane,
                                                      uint32_t sbuf, const CUtensorMap* tmC,
                                                      const GemmParams& p, int32_t row0,
                                                      int32_t x) {
-  if constexpr (kEpiDirect) {
+  if (p.epi_direct) {
     const int32_t row = row0 + static_cast<int32_t>(lane);
     if (row < static_cast<int32_t>(p.M)) {
       char* base = static_cast<char*>(p.C) +

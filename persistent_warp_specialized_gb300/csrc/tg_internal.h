@@ -17,6 +17,7 @@ struct GemmLaunch {
   uint32_t split_from, total_units;
   uint32_t column_major;
   uint32_t dynamic;
+  uint32_t epi_direct;
   uint32_t grid;
   uint64_t watchdog_ns;
   int32_t* trace;

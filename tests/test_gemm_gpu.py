@@ -14,7 +14,8 @@ import persistent_warp_specialized_gb300 as tg
 from persistent_warp_specialized_gb300 import workloads as wl
 from oracle import formats
 
-from gpu_helpers import VARIANTS, assert_within_tolerance, ensure_library, oracle_bits, run_gpu
+from gpu_helpers import (VARIANTS, assert_within_tolerance, ensure_library, nan_filled, oracle_bits,
+                         run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -179,3 +180,26 @@ def test_rejections_with_a_gpu():
         tg.tg_gemm_persistent(big.data_ptr() + 2, b, a, 64, 64, 64, "bf16")
     assert e.value.code == tg.TG_ERR_ALIGN
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("M,N,K", [(1000, 520, 384), (4000, 7000, 512), (300, 2056, 136),
+                                   (8192, 8192, 256)])
+def test_direct_store_epilogue_is_bit_exact(M, N, K, variant):
+    # TG_EPILOGUE_DIRECT: 16-byte stores from registers, clipped at M and N by the kernel
+    a, b = wl.small_int_inputs(M, N, K, "bf16", seed=M + K)
+    c = nan_filled(M, N, "bf16")
+    tg.tg_gemm_persistent_ex(a.cuda(), b.cuda(), c, M, N, K, "bf16", variant=variant, direct=True)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_direct_store_epilogue_fp16_within_tolerance(variant):
+    M, N, K = 1024, 1024, 1024
+    a, b = wl.make_inputs(M, N, K, "f16", "uniform", seed=2)
+    c = nan_filled(M, N, "f16")
+    tg.tg_gemm_persistent_ex(a.cuda(), b.cuda(), c, M, N, K, "f16", variant=variant, direct=True)
+    torch.cuda.synchronize()
+    assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "f16"), "f16", "direct epilogue")
