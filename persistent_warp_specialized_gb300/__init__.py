@@ -298,3 +298,21 @@ def gemm(a, b, out=None, stream=None):
         out = torch.empty((M, N), dtype=a.dtype, device=a.device)
     tg_gemm_persistent(a, b, out, M, N, K, names[a.dtype], stream)
     return out
+
+
+def mxfp8_gemm(a, sa, b, sb, out=None, out_dtype="bf16", stream=None):
+    """torch convenience: the block-scaled MXFP8 product of CUDA uint8 tensors a [M, K] and
+    b [N, K] (E4M3) with row-major E8M0 scales sa [M, K/32] and sb [N, K/32]; packs the scales
+    (tg_mxfp8_pack_scales) and runs tg_gemm_mxfp8 into ``out`` (a new [M, N] tensor if None)."""
+    import torch
+
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K or tuple(sa.shape) != (M, K // 32) or tuple(sb.shape) != (N, K // 32):
+        raise ValueError("shapes: a [M, K], b [N, K], sa [M, K/32], sb [N, K/32]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float16,
+                          device=a.device)
+    tg_gemm_mxfp8(a, mxfp8_pack(sa, K, stream), b, mxfp8_pack(sb, K, stream), out, M, N, K,
+                  out_dtype, stream)
+    return out

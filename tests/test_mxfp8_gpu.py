@@ -212,3 +212,12 @@ def test_group_width_option_followed(variant):
     for u in range(units):
         assert tuple(int(v) for v in got[u]) == by_unit[u], u
     assert np.array_equal(got_c, ref_bits(a, sa, b, sb))
+
+
+def test_mxfp8_gemm_convenience_matches_the_oracle():
+    M, N, K = 300, 520, 256
+    a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=4)
+    c = tg.mxfp8_gemm(a.cuda(), sa.cuda(), b.cuda(), sb.cuda())
+    torch.cuda.synchronize()
+    assert c.shape == (M, N) and c.dtype == torch.bfloat16
+    assert np.array_equal(wl.bits(c.cpu()), ref_bits(a, sa, b, sb))
