@@ -6,6 +6,7 @@
 #include "tg_gemm_pair_kernel.cuh"
 #include "tg_internal.h"
 #include "tg_mx_kernel.cuh"
+#include "tg_mx_pack.cuh"
 #include "tg_mx_pair_kernel.cuh"
 
 namespace tg {
@@ -195,11 +196,9 @@ cudaError_t launch_mxfp8(int out_dtype, bool debug, int variant, const MxLaunch&
 
 cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_blocks,
                            uint32_t row_blocks, cudaStream_t stream) {
-  const uint64_t words = static_cast<uint64_t>(k_blocks) * row_blocks * kBM;
-  if (words == 0) return cudaSuccess;
-  uint64_t blocks = (words + 255) / 256;
-  if (blocks > 8192) blocks = 8192;
-  mx_pack_scales_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  if (k_blocks == 0 || row_blocks == 0) return cudaSuccess;
+  const dim3 grid(row_blocks, (k_blocks + kMxPackKb - 1) / kMxPackKb);
+  mx_pack_scales_kernel<<<grid, kMxPackThreads, 0, stream>>>(
       static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, k_blocks, row_blocks);
   return cudaGetLastError();
 }

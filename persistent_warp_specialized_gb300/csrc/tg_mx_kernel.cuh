@@ -291,24 +291,4 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Packs row-major scales sf [rows, K / 32] into atoms: out[(k * row_blocks + b) * 512 +
-// (r % 32) * 16 + (r / 32) * 4 + j] = sf[b * 128 + r, 4k + j] (0 for rows >= rows), for every
-// k-block k < K / 128, row block b < row_blocks and r < 128.  One thread per 4-byte word.
-__global__ void mx_pack_scales_kernel(const uint8_t* __restrict__ sf, uint8_t* __restrict__ out,
-                                      uint32_t rows, uint32_t k_blocks, uint32_t row_blocks) {
-  const uint64_t words = static_cast<uint64_t>(k_blocks) * row_blocks * kBM;
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  const uint64_t row_bytes = static_cast<uint64_t>(k_blocks) * 4u;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
-       i += stride) {
-    const uint32_t r = static_cast<uint32_t>(i % kBM);
-    const uint64_t kb = i / kBM;                    // k * row_blocks + b
-    const uint32_t b = static_cast<uint32_t>(kb % row_blocks);
-    const uint32_t k = static_cast<uint32_t>(kb / row_blocks);
-    const uint32_t row = b * kBM + r;
-    const uint32_t v = row < rows ? *reinterpret_cast<const uint32_t*>(sf + row * row_bytes + 4u * k) : 0u;
-    *reinterpret_cast<uint32_t*>(out + kb * kMxSfAtomBytes + (r % 32u) * 16u + (r / 32u) * 4u) = v;
-  }
-}
-
 }  // namespace tg
