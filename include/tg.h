@@ -131,6 +131,30 @@ int tg_tile_schedule(int m_blocks, int n_blocks, int num_sms, int group, int32_t
 int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int flags,
                         int32_t* out_host);
 
+/*
+ * tg_tile_schedule_noalloc -- tg_tile_schedule_ex without any device allocation.  The pages
+ * have no counterpart of this call; it is an addition of this library.
+ *   tg_tile_schedule and tg_tile_schedule_ex stage their rows in a device buffer that they
+ *   allocate and free inside the call.  Not every caller can let a library do that: a process
+ *   whose device memory is all handed out by its own pool allocator (a fresh cudaMalloc can fail
+ *   there, or take memory the pool counts on), or a host thread that must not stall, since
+ *   cudaFree waits for all work on the device.  This call stages the rows in a fixed array that
+ *   is part of the library's device image instead, TG_SCHEDULE_NOALLOC_MAX_UNITS rows of 5
+ *   int32 (1.25 MiB), which every GPU that loads the library holds until the process exits;
+ *   it calls no allocation routine.
+ *   Arguments, flags, rows and return value: as tg_tile_schedule_ex.  A call with more than
+ *   TG_SCHEDULE_NOALLOC_MAX_UNITS units returns TG_ERR_ARG before it touches the device.
+ *   The first call on a device looks up the array's address there (with that device current):
+ *   make that first call before any stream capture.  All calls on a device share the one array,
+ *   so calls that overlapped on the GPU would race; each call therefore holds a process-wide
+ *   lock from its launch until its rows are on the host, and returns only then (legacy default
+ *   stream).  Nothing needs clearing between calls: every row copied back is written by the
+ *   call that copies it.
+ */
+#define TG_SCHEDULE_NOALLOC_MAX_UNITS 65536
+int tg_tile_schedule_noalloc(int m_blocks, int n_blocks, int num_sms, int group, int flags,
+                             int32_t* out_host);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* tg_last_error(void);
 

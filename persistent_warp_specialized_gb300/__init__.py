@@ -30,6 +30,7 @@ TG_SCHEDULE_COLUMN_MAJOR = 0x200
 TG_SCHEDULE_SPLIT_TAIL = 0x1
 TG_SCHEDULE_DYNAMIC = 0x400
 TG_EPILOGUE_DIRECT = 0x800
+TG_SCHEDULE_NOALLOC_MAX_UNITS = 65536   # scratch rows of tg_tile_schedule_noalloc
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
@@ -39,6 +40,7 @@ EXPORTED = (
     "tg_gemm_persistent_ex",
     "tg_tile_schedule",
     "tg_tile_schedule_ex",
+    "tg_tile_schedule_noalloc",
     "tg_last_error",
     "tg_gemm_config",
     "tg_gemm_launch_shape",
@@ -80,6 +82,9 @@ def load_library(path=LIB_PATH):
     lib.tg_tile_schedule.restype = i32
     lib.tg_tile_schedule_ex.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.tg_tile_schedule_ex.restype = i32
+    lib.tg_tile_schedule_noalloc.argtypes = [i32, i32, i32, i32, i32,
+                                             ctypes.POINTER(ctypes.c_int32)]
+    lib.tg_tile_schedule_noalloc.restype = i32
     lib.tg_last_error.argtypes = []
     lib.tg_last_error.restype = ctypes.c_char_p
     ip = ctypes.POINTER(ctypes.c_int)
@@ -231,6 +236,20 @@ def tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, split_tail=True, col
     flags = (TG_SCHEDULE_SPLIT_TAIL if split_tail else 0) | (
         TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
     n = _check(load_library().tg_tile_schedule_ex(m_blocks, n_blocks, num_sms, group, flags, buf))
+    return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
+
+
+def tg_tile_schedule_noalloc(m_blocks, n_blocks, num_sms, group, split_tail=True,
+                             column_major=False):
+    """The rows of tg_tile_schedule_ex, from the entry point that allocates no device memory
+    (for callers whose device memory is all owned by their own allocator, or that must not
+    stall on cudaFree).  At most TG_SCHEDULE_NOALLOC_MAX_UNITS units."""
+    rows = min(2 * max(0, m_blocks) * max(0, n_blocks), TG_SCHEDULE_NOALLOC_MAX_UNITS)
+    buf = (ctypes.c_int32 * (5 * max(rows, 1)))()
+    flags = (TG_SCHEDULE_SPLIT_TAIL if split_tail else 0) | (
+        TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
+    n = _check(load_library().tg_tile_schedule_noalloc(m_blocks, n_blocks, num_sms, group, flags,
+                                                       buf))
     return [tuple(buf[5 * i: 5 * i + 5]) for i in range(n)]
 
 

@@ -426,6 +426,19 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
 
 }  // namespace
 
+// Scratch of tg_tile_schedule_noalloc: TG_SCHEDULE_NOALLOC_MAX_UNITS rows of 5 int32 in the
+// library's device image, so that call needs no allocation.  In host code the name stands for a
+// host-side shadow, not a device address: the device address is looked up once per device with
+// cudaGetSymbolAddress and passed to the scheduler kernel.
+static __device__ __align__(256) int32_t g_schedule_scratch[5 * TG_SCHEDULE_NOALLOC_MAX_UNITS];
+
+namespace {
+
+int32_t* g_schedule_scratch_dev[kMaxDevices];   // per device: address of g_schedule_scratch
+std::mutex g_schedule_scratch_mu;               // one call at a time uses the array
+
+}  // namespace
+
 extern "C" {
 
 int64_t tg_mxfp8_scale_bytes(int64_t rows, int64_t K) {
@@ -586,6 +599,42 @@ int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int 
     tg::PersistentTileScheduler::tail_split(tiles, uint32_t(num_sms), first, units);
   return schedule_rows(m_blocks, n_blocks, num_sms, group, first, units,
                        (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u, 5, out_host);
+}
+
+int tg_tile_schedule_noalloc(int m_blocks, int n_blocks, int num_sms, int group, int flags,
+                             int32_t* out_host) {
+  int rc = check_schedule_args(m_blocks, n_blocks, num_sms, group, out_host);
+  if (rc != TG_OK) return rc;
+  if (flags & ~(TG_SCHEDULE_SPLIT_TAIL | TG_SCHEDULE_COLUMN_MAJOR))
+    return fail(TG_ERR_ARG, "unknown schedule flags 0x%x", flags);
+  const uint32_t tiles = uint32_t(m_blocks) * uint32_t(n_blocks);
+  uint32_t first = tiles, units = tiles;
+  if (flags & TG_SCHEDULE_SPLIT_TAIL)
+    tg::PersistentTileScheduler::tail_split(tiles, uint32_t(num_sms), first, units);
+  if (units > TG_SCHEDULE_NOALLOC_MAX_UNITS)
+    return fail(TG_ERR_ARG,
+                "tg_tile_schedule_noalloc: %u units exceed its fixed scratch of %d units "
+                "(use tg_tile_schedule_ex)",
+                units, TG_SCHEDULE_NOALLOC_MAX_UNITS);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_CUDA, "device ordinal %d unsupported", dev);
+  std::lock_guard<std::mutex> lock(g_schedule_scratch_mu);
+  int32_t*& scratch = g_schedule_scratch_dev[dev];
+  if (scratch == nullptr) {
+    int32_t* ptr = nullptr;
+    e = cudaGetSymbolAddress((void**)&ptr, g_schedule_scratch);
+    if (e != cudaSuccess) return fail_cuda("address of the schedule scratch", e);
+    scratch = ptr;
+  }
+  e = tg::launch_tile_schedule(uint32_t(m_blocks), uint32_t(n_blocks), uint32_t(num_sms),
+                               uint32_t(group), first, units,
+                               (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u, scratch, nullptr);
+  if (e != cudaSuccess) return fail_cuda("tile schedule", e);
+  e = cudaMemcpy(out_host, scratch, uint64_t(units) * 5 * sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda("copy of the schedule to the host", e);
+  return static_cast<int>(units);
 }
 
 const char* tg_last_error(void) { return g_err; }
