@@ -2,6 +2,8 @@
 // the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
 // block-scaled MXFP8 GEMM (single CTA and CTA pair), the tile-schedule inspection kernel, and the zero fill used when
 // K == 0.  All kernels share this translation unit's watchdog status word.
+#include <utility>
+
 #include "tg_gemm_kernel.cuh"
 #include "tg_gemm_pair_kernel.cuh"
 #include "tg_internal.h"
@@ -67,18 +69,37 @@ GemmParams params_of(const GemmLaunch& l) {
   return p;
 }
 
+// Launches ``kernel`` with programmatic stream serialization: it may be scheduled while the
+// previous kernel in the stream is still finishing (as that kernel's CTAs exit).  Every kernel
+// launched this way issues griddepcontrol.wait before its first global memory access, so the
+// stream's ordering of memory effects is unchanged; what overlaps is the launch itself and each
+// CTA's set-up (barriers, TMEM allocation, descriptor prefetch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, uint32_t threads, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int DT, bool DEBUG>
 cudaError_t launch_one(const GemmLaunch& l, cudaStream_t stream) {
-  gemm_persistent_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, params_of(l));
-  return cudaGetLastError();
+  return launch_pdl(gemm_persistent_ws_kernel<DT, DEBUG>, l.grid, kThreads, kSmemBytes, stream,
+                    l.tmA, l.tmB, l.tmC, params_of(l));
 }
 
 template <int DT, bool DEBUG>
 cudaError_t launch_pair(const GemmLaunch& l, cudaStream_t stream) {
-  gemm_pair_ws_kernel<DT, DEBUG><<<l.grid, kThreads, kPairSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, params_of(l));
-  return cudaGetLastError();
+  return launch_pdl(gemm_pair_ws_kernel<DT, DEBUG>, l.grid, kThreads, kPairSmemBytes, stream,
+                    l.tmA, l.tmB, l.tmC, params_of(l));
 }
 
 template <int DT, bool DEBUG>
@@ -116,16 +137,14 @@ MxParams mx_params_of(const MxLaunch& l) {
 
 template <int OUT, bool DEBUG>
 cudaError_t launch_mx(const MxLaunch& l, cudaStream_t stream) {
-  gemm_mxfp8_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, mx_params_of(l));
-  return cudaGetLastError();
+  return launch_pdl(gemm_mxfp8_ws_kernel<OUT, DEBUG>, l.grid, kThreads, kMxSmemBytes, stream,
+                    l.tmA, l.tmB, l.tmC, mx_params_of(l));
 }
 
 template <int OUT, bool DEBUG>
 cudaError_t launch_mx_pair(const MxLaunch& l, cudaStream_t stream) {
-  gemm_mxfp8_pair_ws_kernel<OUT, DEBUG><<<l.grid, kThreads, kMxPairSmemBytes, stream>>>(
-      l.tmA, l.tmB, l.tmC, l.tmSFA, l.tmSFB, mx_params_of(l));
-  return cudaGetLastError();
+  return launch_pdl(gemm_mxfp8_pair_ws_kernel<OUT, DEBUG>, l.grid, kThreads, kMxPairSmemBytes,
+                    stream, l.tmA, l.tmB, l.tmC, l.tmSFA, l.tmSFB, mx_params_of(l));
 }
 
 template <int OUT, bool DEBUG>
@@ -198,9 +217,9 @@ cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_
                            uint32_t row_blocks, cudaStream_t stream) {
   if (k_blocks == 0 || row_blocks == 0) return cudaSuccess;
   const dim3 grid(row_blocks, (k_blocks + kMxPackKb - 1) / kMxPackKb);
-  mx_pack_scales_kernel<<<grid, kMxPackThreads, 0, stream>>>(
-      static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, k_blocks, row_blocks);
-  return cudaGetLastError();
+  return launch_pdl(mx_pack_scales_kernel, grid, kMxPackThreads, 0, stream,
+                    static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, k_blocks,
+                    row_blocks);
 }
 
 cudaError_t launch_zero_fill(void* C, uint64_t bytes, cudaStream_t stream) {

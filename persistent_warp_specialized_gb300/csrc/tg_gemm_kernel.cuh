@@ -277,6 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tcgen05_fence_before_sync();
   __syncthreads();
   tcgen05_fence_after_sync();
+  // Launched with programmatic stream serialization: this CTA may start while the previous
+  // kernel in the stream is finishing.  Nothing above touches global memory; nothing below
+  // runs before that kernel has completed.  Then the next launch may be scheduled.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   const uint32_t tmem_base = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort;

@@ -11,6 +11,7 @@
 #include <cstdint>
 
 #include "tg_config.h"
+#include "tg_ptx.cuh"
 
 namespace tg {
 
@@ -22,6 +23,8 @@ __global__ void __launch_bounds__(kMxPackThreads)
                           uint32_t rows, uint32_t k_blocks, uint32_t row_blocks) {
   // words of k-block j of the tile, in atom order: word t = row (t % 4) * 32 + t / 4
   __shared__ uint32_t tile[kMxPackKb][kBM];
+  grid_dependency_wait();      // launched like the GEMM kernels (programmatic serialization)
+  grid_launch_dependents();
   const uint32_t b = blockIdx.x;                       // row block
   const uint32_t k0 = blockIdx.y * kMxPackKb;          // first k-block of the tile
   const uint64_t row_bytes = static_cast<uint64_t>(k_blocks) * 4u;

@@ -454,4 +454,15 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t m, uint32_t n, uint32
   return (b_sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (a_sf_id << 29);
 }
 
+// Programmatic dependent launch.  griddepcontrol.wait blocks until every grid this launch
+// depends on has completed and its memory operations are visible (it returns at once when the
+// launch had no programmatic dependency); griddepcontrol.launch_dependents lets the next
+// launch in the stream be scheduled once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace tg
