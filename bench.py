@@ -232,6 +232,21 @@ def oracle_slab(a_bits, b_bits, fmt, rows):
     return ogemm.gemm_ref(a_bits[:rows], b_bits, fmt)
 
 
+def timed_oracle_sample(run, M, seconds):
+    """Run ``run(rows)`` (the oracle on rows [0, rows) of C) on growing samples until one takes
+    at least half of ``seconds`` or covers all M rows; return (rows, seconds taken, result) of
+    that last run.  Each oracle call has a fixed part (decoding all of B) that a small probe
+    would wrongly count per row."""
+    rows = min(M, 32)
+    while True:
+        t0 = time.perf_counter()
+        out = run(rows)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * seconds or rows >= M:
+            return rows, dt, out
+        rows = min(M, int(rows * min(8.0, max(2.0, seconds / max(dt, 1e-6)))))
+
+
 def calibrate_rows(a_bits, b_bits, fmt, seconds):
     """Rows of C the oracle computes in about ``seconds`` (at least 8)."""
     M = a_bits.shape[0]
@@ -439,10 +454,8 @@ def run_tg(args):
         from oracle import formats
 
         a_bits, b_bits = wl.bits(a_cpu), wl.bits(b_cpu)
-        rows = calibrate_rows(a_bits, b_bits, w.dtype, args.cpu_seconds)
-        t_0 = time.perf_counter()
-        ref = oracle_slab(a_bits, b_bits, w.dtype, rows)
-        dt = time.perf_counter() - t_0
+        rows, dt, ref = timed_oracle_sample(lambda r: oracle_slab(a_bits, b_bits, w.dtype, r),
+                                            w.M, args.cpu_seconds)
         got = formats.decode(wl.bits(c[:rows].cpu()), w.dtype)
         want = formats.decode(ref, w.dtype)
         err = np.abs(got - want)
@@ -611,13 +624,8 @@ def run_tg_mx(args):
         from oracle import formats
 
         an, san, bn, sbn = (t.numpy() for t in host)
-        probe = 16
-        t_0 = time.perf_counter()
-        mx_oracle_slab(an, san, bn, sbn, probe)
-        rows = int(max(min(M, probe * args.cpu_seconds / max(time.perf_counter() - t_0, 1e-6)), 8))
-        t_0 = time.perf_counter()
-        ref = mx_oracle_slab(an, san, bn, sbn, rows)
-        dt = time.perf_counter() - t_0
+        rows, dt, ref = timed_oracle_sample(lambda r: mx_oracle_slab(an, san, bn, sbn, r), M,
+                                            args.cpu_seconds)
         got = formats.decode(wl.bits(c[:rows].cpu()), "bf16")
         want = formats.decode(ref, "bf16")
         err = np.abs(got - want)

@@ -111,3 +111,23 @@ def test_mxfp8_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["config"]["workload"] == "mxfp8_512" and d["config"]["in_dtype"] == "e4m3"
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_oracle_sample_grows_past_the_fixed_cost_of_a_call():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # every call costs 30 ms plus 0.1 ms per row: a 32-row probe would predict ~1 ms per row
+    calls = []
+
+    def run(rows):
+        calls.append(rows)
+        time.sleep(0.03 + 1e-4 * rows)
+        return rows
+
+    rows, dt, out = bench.timed_oracle_sample(run, 100000, 0.4)
+    assert out == rows == calls[-1]
+    assert dt >= 0.2
+    assert rows > 32 * 0.4 / (0.03 + 32e-4)    # more than the one-probe estimate
+    rows, dt, out = bench.timed_oracle_sample(run, 200, 10.0)
+    assert rows == 200                        # never beyond M
