@@ -247,14 +247,17 @@ def timed_oracle_sample(run, M, seconds):
         rows = min(M, int(rows * min(8.0, max(2.0, seconds / max(dt, 1e-6)))))
 
 
-def calibrate_rows(a_bits, b_bits, fmt, seconds):
-    """Rows of C the oracle computes in about ``seconds`` (at least 8)."""
-    M = a_bits.shape[0]
-    probe = min(M, 32)
-    t0 = time.perf_counter()
-    oracle_slab(a_bits, b_bits, fmt, probe)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    return int(max(min(M, probe * seconds / dt), min(M, 8)))
+def block_side(run, limit, seconds):
+    """Side r of the square block C[:r, :r] that ``run(r)`` (the oracle on that block: r rows
+    of A, r columns of B) computes in about ``seconds``; r doubles from 64 until one run takes
+    at least half of that, so calibrating costs about one step."""
+    r = min(limit, 64)
+    while True:
+        t0 = time.perf_counter()
+        run(r)
+        if time.perf_counter() - t0 >= 0.5 * seconds or r >= limit:
+            return r
+        r = min(limit, 2 * r)
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -269,17 +272,22 @@ def run_reference(args):
     a_bits, b_bits = wl.bits(a), wl.bits(b)
     steps, warm = max(1, args.steps), max(0, args.warmup)
     per_step = max(0.05, min(2.0, 150.0 / (steps + warm)))
-    rows = calibrate_rows(a_bits, b_bits, w.dtype, per_step)
+
+    def block(r):
+        from oracle import gemm as ogemm
+
+        return ogemm.gemm_ref(a_bits[:r], b_bits[:, :r], w.dtype)
+
+    r = block_side(block, min(w.M, w.N), per_step)
     for _ in range(warm):
-        oracle_slab(a_bits, b_bits, w.dtype, rows)
+        block(r)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle_slab(a_bits, b_bits, w.dtype, rows)
+        block(r)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * w.N * w.K * steps
-    value = flops / dt / 1e12
-    sample = (f"rows [0, {rows}) of C = A.B for {w.name} ({rows} x {w.N} outputs, K={w.K}) per step: "
-              f"decode, binary64 product, round to {w.dtype}")
+    value = 2.0 * r * r * w.K * steps / dt / 1e12
+    sample = (f"block C[:{r}, :{r}] of C = A.B for {w.name} ({r} x {r} outputs, K={w.K}) per "
+              f"step: decode, binary64 product, round to {w.dtype}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
@@ -506,18 +514,21 @@ def run_reference_mx(args):
     a, sa, b, sb = (t.numpy() for t in wl.make_mx_inputs(M, N, K, seed))
     steps, warm = max(1, args.steps), max(0, args.warmup)
     per_step = max(0.05, min(2.0, 150.0 / (steps + warm)))
-    probe = 16
-    t0 = time.perf_counter()
-    mx_oracle_slab(a, sa, b, sb, probe)
-    rows = int(max(min(M, probe * per_step / max(time.perf_counter() - t0, 1e-6)), 8))
+
+    def block(r):
+        from oracle import mx
+
+        return mx.gemm_mxfp8_ref(a[:r], sa[:r], b[:r], sb[:r], "bf16")
+
+    r = block_side(block, min(M, N), per_step)
     for _ in range(warm):
-        mx_oracle_slab(a, sa, b, sb, rows)
+        block(r)
     t0 = time.perf_counter()
     for _ in range(steps):
-        mx_oracle_slab(a, sa, b, sb, rows)
+        block(r)
     dt = time.perf_counter() - t0
-    value = 2.0 * rows * N * K * steps / dt / 1e12
-    sample = (f"rows [0, {rows}) of the MXFP8 product ({rows} x {N} outputs, K={K}) per step: "
+    value = 2.0 * r * r * K * steps / dt / 1e12
+    sample = (f"block C[:{r}, :{r}] of the MXFP8 product ({r} x {r} outputs, K={K}) per step: "
               f"decode, scale, binary64 product, round to bf16")
     print(json.dumps({
         "impl": "reference", "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world,

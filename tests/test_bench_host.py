@@ -131,3 +131,19 @@ def test_oracle_sample_grows_past_the_fixed_cost_of_a_call():
     assert rows > 32 * 0.4 / (0.03 + 32e-4)    # more than the one-probe estimate
     rows, dt, out = bench.timed_oracle_sample(run, 200, 10.0)
     assert rows == 200                        # never beyond M
+
+
+def test_reference_block_side_bounds_one_step():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # a call costs 1 ms per unit of r (the operand decode) plus r^2 / 4e6 s (the product)
+    def run(r):
+        time.sleep(1e-6 * r + r * r / 4e6)
+
+    r = bench.block_side(run, 8192, 0.2)
+    t0 = time.perf_counter()
+    run(r)
+    dt = time.perf_counter() - t0
+    assert 0.1 <= dt <= 0.9
+    assert bench.block_side(run, 100, 5.0) == 100     # never beyond the matrix
