@@ -22,7 +22,10 @@
  *     padding: the row stride of A is K elements, of B and C it is N elements.
  *   - ``stream`` is a cudaStream_t (NULL = the legacy default stream).  GEMM entry points
  *     are asynchronous: TG_OK means the work was enqueued; faults during execution surface
- *     at the caller's next synchronisation, as with any CUDA launch.
+ *     at the caller's next synchronisation, as with any CUDA launch.  The GEMM and scale-pack
+ *     kernels are launched with programmatic dependent launch: their CTAs may start while the
+ *     previous kernel in the stream is finishing, but wait for it to complete before their
+ *     first access to global memory, so the stream's order of memory effects is kept.
  *   - A negative return is an error; tg_last_error() then holds a message (thread-local;
  *     valid until the next call on the same thread).  On error nothing was enqueued.
  */
