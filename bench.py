@@ -43,7 +43,7 @@ NOMINAL_DENSE_BF16_TFLOPS = 2250.0       # GB300 dense bf16/fp16, no sparsity
 DENSE_FLOP_PER_CLK_PER_SM = 8192         # derived: one 128x256x16 MMA per 128 cycles
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILES = os.path.join(ROOT, "profiles")
-KERNEL_NAMES = {1: "gemm_persistent_ws", 2: "gemm_pair_ws"}   # by tg variant
+KERNEL_NAMES = {1: "gemm_persistent_ws", 2: "gemm_pair_ws", 3: "gemm_pair_wide_ws"}   # by tg variant
 
 
 def parse_args(argv=None):
@@ -53,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
     ap.add_argument("--workload", default="gemm_8192_bf16")
-    ap.add_argument("--variant", choices=["auto", "single", "pair"], default="auto",
+    ap.add_argument("--variant", choices=["auto", "single", "pair", "wide"], default="auto",
                     help="kernel variant (auto: the library's choice, as tg_gemm_persistent)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -579,6 +579,10 @@ def run_tg_mx(args):
         gemm_only()
 
     launch = tg.tg_gemm_launch_shape(M, N, K, args.variant)   # the GEMM's kernel and launch
+    if launch["variant"] == tg.TG_VARIANT_PAIR_WIDE:
+        # the wide pair kernel is dense-only; where the dense choice is wide, the MXFP8
+        # choice is the pair kernel (its 256 x 256 tiles then fill more than a wave)
+        launch = tg.tg_gemm_launch_shape(M, N, K, "pair")
     kernel = "gemm_mxfp8_pair_ws" if launch["variant"] == tg.TG_VARIANT_PAIR else "gemm_mxfp8_ws"
 
     steps, warm = max(1, args.steps), max(3, args.warmup)

@@ -47,6 +47,9 @@ enum {
   TG_VARIANT_SINGLE = 1,  /* one CTA per 128 x 256 output tile, tcgen05 cta_group::1 */
   TG_VARIANT_PAIR = 2,    /* a CTA pair per 256 x 256 output tile, tcgen05 cta_group::2
                              ("[Feature] Introduce tile scheduler #2441", gemm_persistent_2cta) */
+  TG_VARIANT_PAIR_WIDE = 3, /* dense GEMM only: a CTA pair per 256 x 512 output tile, as two
+                               N-halves of 256 into the two halves of TMEM (one accumulator),
+                               block_K 64 x 4 stages; A is loaded once per 512 columns */
   /* OR'ed into a variant: walk tiles exactly as the page's scheduler does.  By default, when
      the last partial wave of tiles would keep at most half of the workers busy, each of its
      tiles is cut into two half-width (N) units so that wave takes half a tile's time; see
@@ -99,7 +102,10 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
 /*
  * tg_gemm_persistent_ex -- tg_gemm_persistent with an explicit kernel variant (TG_VARIANT_*).
  * Same arguments, rules and results; TG_ERR_ARG for an unknown variant.  The pair variant
- * walks ceil(M/256) x ceil(N/256) tiles with one scheduler worker per CTA pair.
+ * walks ceil(M/256) x ceil(N/256) tiles with one scheduler worker per CTA pair, the wide pair
+ * variant ceil(M/256) x ceil(N/512) tiles (its tail-split half units are 256 x 256).
+ * TG_VARIANT_AUTO takes the wide pair variant when its tiles fill at least four waves of
+ * resident pairs, else the pair variant when its tiles fill at least one, else the single one.
  */
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
                           int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant);

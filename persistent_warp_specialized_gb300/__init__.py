@@ -25,13 +25,15 @@ TG_ERR_TIMEOUT = -4
 TG_VARIANT_AUTO = 0
 TG_VARIANT_SINGLE = 1
 TG_VARIANT_PAIR = 2
+TG_VARIANT_PAIR_WIDE = 3
 TG_SCHEDULE_PLAIN = 0x100
 TG_SCHEDULE_COLUMN_MAJOR = 0x200
 TG_SCHEDULE_SPLIT_TAIL = 0x1
 TG_SCHEDULE_DYNAMIC = 0x400
 TG_EPILOGUE_DIRECT = 0x800
 TG_SCHEDULE_NOALLOC_MAX_UNITS = 65536   # scratch rows of tg_tile_schedule_noalloc
-VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR}
+VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR,
+            "wide": TG_VARIANT_PAIR_WIDE}
 
 DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
 
@@ -166,7 +168,7 @@ def _group(g):
 
 
 def _variant(v, plain=False, column_major=False, dynamic=False, group=None, direct=False):
-    """"auto" / "single" / "pair" (or a TG_VARIANT_* int) plus the schedule flags."""
+    """"auto" / "single" / "pair" / "wide" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
     return (code | (TG_SCHEDULE_PLAIN if plain else 0)
             | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
@@ -176,7 +178,7 @@ def _variant(v, plain=False, column_major=False, dynamic=False, group=None, dire
 
 def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
                           column_major=False, dynamic=False, group=None, direct=False):
-    """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair");
+    """tg_gemm_persistent with an explicit kernel variant ("auto", "single", "pair", "wide");
     ``plain`` walks the page's tile order with no tail split; ``column_major`` the scheduler's
     column-major order."""
     return _check(load_library().tg_gemm_persistent_ex(

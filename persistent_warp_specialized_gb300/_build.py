@@ -60,6 +60,9 @@ KERNEL_SOURCES = {
                            "tg_gemm_kernel.cuh"],
     "gemm_pair_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
                      "tg_gemm_pair_kernel.cuh"],
+    "gemm_pair_wide_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
+                          "tg_gemm_pair_kernel.cuh", "tg_wide_config.h",
+                          "tg_gemm_pair_wide_kernel.cuh"],
     "gemm_mxfp8_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh", "tg_gemm_kernel.cuh",
                       "tg_mx_kernel.cuh"],
     "gemm_mxfp8_pair_ws": ["tg_config.h", "tg_ptx.cuh", "tg_tile_scheduler.cuh",

@@ -1,11 +1,13 @@
 // tg_gemm.cu -- instantiations and launchers of the sm_103a kernels behind the C ABI:
-// the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds), the
+// the persistent warp-specialized GEMM (fp16 and bf16, product and debug builds; single CTA,
+// CTA pair and wide CTA pair), the
 // block-scaled MXFP8 GEMM (single CTA and CTA pair), the tile-schedule inspection kernel, and the zero fill used when
 // K == 0.  All kernels share this translation unit's watchdog status word.
 #include <utility>
 
 #include "tg_gemm_kernel.cuh"
 #include "tg_gemm_pair_kernel.cuh"
+#include "tg_gemm_pair_wide_kernel.cuh"
 #include "tg_internal.h"
 #include "tg_mx_kernel.cuh"
 #include "tg_mx_pack.cuh"
@@ -103,14 +105,24 @@ cudaError_t launch_pair(const GemmLaunch& l, cudaStream_t stream) {
 }
 
 template <int DT, bool DEBUG>
+cudaError_t launch_pair_wide(const GemmLaunch& l, cudaStream_t stream) {
+  return launch_pdl(gemm_pair_wide_ws_kernel<DT, DEBUG>, l.grid, kThreads, kWideSmemBytes, stream,
+                    l.tmA, l.tmB, l.tmC, params_of(l));
+}
+
+template <int DT, bool DEBUG>
 cudaError_t set_smem_attr() {
   cudaError_t e = cudaFuncSetAttribute(gemm_persistent_ws_kernel<DT, DEBUG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_pair_ws_kernel<DT, DEBUG>,
+  e = cudaFuncSetAttribute(gemm_pair_ws_kernel<DT, DEBUG>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPairSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_pair_wide_ws_kernel<DT, DEBUG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kPairSmemBytes));
+                              static_cast<int>(kWideSmemBytes));
 }
 
 MxParams mx_params_of(const MxLaunch& l) {
@@ -181,9 +193,13 @@ cudaError_t prepare_gemm_kernels(int* max_pairs) {
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0, mx_clusters = 0;
+  int clusters = 0, mx_clusters = 0, wide_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_ws_kernel<1, false>, &cfg);
   if (e != cudaSuccess) return e;
+  cfg.dynamicSmemBytes = kWideSmemBytes;
+  e = cudaOccupancyMaxActiveClusters(&wide_clusters, gemm_pair_wide_ws_kernel<1, false>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (wide_clusters < clusters) clusters = wide_clusters;
   cfg.dynamicSmemBytes = kMxPairSmemBytes;
   e = cudaOccupancyMaxActiveClusters(&mx_clusters, gemm_mxfp8_pair_ws_kernel<1, false>, &cfg);
   if (e != cudaSuccess) return e;
@@ -197,6 +213,11 @@ cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
     if (dtype == 0)
       return debug ? launch_pair<0, true>(l, stream) : launch_pair<0, false>(l, stream);
     return debug ? launch_pair<1, true>(l, stream) : launch_pair<1, false>(l, stream);
+  }
+  if (variant == kVariantPairWide) {
+    if (dtype == 0)
+      return debug ? launch_pair_wide<0, true>(l, stream) : launch_pair_wide<0, false>(l, stream);
+    return debug ? launch_pair_wide<1, true>(l, stream) : launch_pair_wide<1, false>(l, stream);
   }
   if (dtype == 0) return debug ? launch_one<0, true>(l, stream) : launch_one<0, false>(l, stream);
   return debug ? launch_one<1, true>(l, stream) : launch_one<1, false>(l, stream);

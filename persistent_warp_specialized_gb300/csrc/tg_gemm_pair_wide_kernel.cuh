@@ -1,0 +1,277 @@
+// tg_gemm_pair_wide_kernel.cuh -- the CTA-pair GEMM with 256 x 512 output tiles.
+//
+// The pair kernel of tg_gemm_pair_kernel.cuh ("[Feature] Introduce tile scheduler #2441",
+// ``gemm_persistent_2cta``) with twice the tile width: one unit is 256 rows x 512 columns,
+// computed as two N-halves of 256 columns, each by tcgen05.mma cta_group::2 M = 256, N = 256,
+// K = 16 into its own half of TMEM (columns 0..255 and 256..511).  Per k-block of 64 each CTA
+// loads one A box 128 x 64 (16 KiB, its 128 rows) and four B boxes 64 x 64 (8 KiB each: its
+// 128 columns of each N-half), 48 KiB per stage, 4 stages.  Against the 256 x 256 pair tile:
+//   * A is loaded once for 512 columns instead of 256: 25 % fewer bytes from L2 into shared
+//     memory per flop;
+//   * a stage holds as much MMA work as the 256 x 256 kernel's 128-deep stage (0.68 us at the
+//     bf16 peak), and a refill has three stages instead of two to arrive;
+//   * the tail split's half units are 256 x 256 (whole N-halves) rather than 256 x 128;
+//   * there is one accumulator (all 512 TMEM columns): the epilogue hands each N-half back on
+//     its own barrier (tmem_empty[h]) once it has read it, and the MMA waits for half h only
+//     before its first write of the next unit.  A half unit hands back its unused half at once,
+//     so both barriers complete once per unit and the parity of unit w is (w & 1) ^ 1.
+// Everything else -- the scheduler, the single iteration clock with slot phase % S, the odd
+// CTA's loads completing on the even CTA's barrier, multicast commits, bounded waits with the
+// pair abort, the TMA-store epilogue -- is the pair kernel's.  Included by exactly one
+// translation unit, after tg_gemm_pair_kernel.cuh.
+#pragma once
+
+#include "tg_gemm_pair_kernel.cuh"
+#include "tg_wide_config.h"
+
+namespace tg {
+
+struct __align__(8) WideCtl {
+  uint64_t loaded[kWideStages];      // used in the even CTA only
+  uint64_t consumed[kWideStages];
+  uint64_t tmem_full;
+  uint64_t tmem_empty[2];            // per N-half; used in the even CTA only (count 256)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// DT: 0 = fp16, 1 = bf16.  p.m_blocks counts 256-row tiles, p.n_blocks 512-column tiles.
+template <int DT, bool DEBUG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_wide_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ WideCtl ctl;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = cluster_ctarank();          // 0: even CTA (issues the MMA), 1: odd
+  const uint32_t pair = blockIdx.x >> 1;
+  const uint32_t num_pairs = gridDim.x >> 1;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA0 = sbase;                 // stage s: A at sA0 + s * kWideStageBytes,
+  const uint32_t sB0 = sbase + kWideABytes;   // then B chunks (2 h + c) of 8 KiB
+  const uint32_t sEpi = sbase + kWideStages * kWideStageBytes;
+
+  const uint32_t bar_loaded = smem_u32(&ctl.loaded[0]);
+  const uint32_t bar_consumed = smem_u32(&ctl.consumed[0]);
+  const uint32_t bar_tmem_full = smem_u32(&ctl.tmem_full);
+  const uint32_t bar_tmem_empty = smem_u32(&ctl.tmem_empty[0]);
+  const uint32_t bar_drain = smem_u32(&ctl.drain);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kWideStages; ++s) {
+      mbar_init(bar_loaded + 8u * s, 1);
+      mbar_init(bar_consumed + 8u * s, 1);
+    }
+    mbar_init(bar_tmem_full, 1);
+    mbar_init(bar_tmem_empty, 2 * kEpiThreads);
+    mbar_init(bar_tmem_empty + 8u, 2 * kEpiThreads);
+    mbar_init(bar_drain, 1);
+    ctl.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  __syncwarp();
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tcgen05_fence_before_sync();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrive or complete_tx
+  tcgen05_fence_after_sync();
+  // Launched with programmatic stream serialization: this CTA may start while the previous
+  // kernel in the stream is finishing.  Nothing above touches global memory; nothing below
+  // runs before that kernel has completed.  Then the next launch may be scheduled.
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&ctl.abort), rank ^ 1u);
+  const uint64_t limit = p.watchdog_ns;
+  const uint64_t k_blocks = p.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units, p.column_major);
+      sched.init(pair);
+      uint32_t pending = 0, pending_par = 0;
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint64_t w = sched.current_iter;
+        const bool half = sched.part >= 0;          // half unit: the N-half ``part`` alone
+        const uint32_t halves = half ? 1u : 2u;
+        const int32_t m0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM);
+        const int32_t n0 = static_cast<int32_t>(sched.n_idx * kWideBN) + (half ? sched.part * kBN : 0);
+        const uint32_t tx_bytes = 2u * (kWideABytes + halves * 2u * kWideBChunkBytes);
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = w * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kWideStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kWideStages) & 1u);
+          if (!pair_wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, peer_abort, limit,
+                                  kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          pending &= ~(1u << s);
+          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
+          if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
+          const int32_t kx = static_cast<int32_t>(k) * kWideBK;
+          tma_load_2d_pair(sA0 + s * kWideStageBytes, &tmA, full_even, kx, m0);
+#pragma unroll
+          for (uint32_t h = 0; h < 2; ++h) {
+            if (h >= halves) break;
+            // CTA r loads columns [128 r, 128 r + 128) of N-half h as two 64-column chunks
+#pragma unroll
+            for (uint32_t c = 0; c < 2; ++c) {
+              const uint32_t dst = sB0 + s * kWideStageBytes + (2u * h + c) * kWideBChunkBytes;
+              const int32_t nx = n0 + static_cast<int32_t>(h * kBN + rank * kPairBNHalf + c * kBChunkCols);
+              tma_load_2d_pair(dst, &tmB, full_even, nx, kx);
+            }
+          }
+          pending |= 1u << s;
+          pending_par = (pending_par & ~(1u << s)) | (par << s);
+        }
+        sched.next_tile();
+      }
+      if (!ok) {
+        if (rank == 0) {
+          for (uint32_t s = 0; s < kWideStages; ++s)
+            if ((pending >> s) & 1u)
+              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
+        } else if (pending) {
+          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
+          // give them time to land before this CTA may leave
+          spin_ns(limit < 1000000ull ? limit : 1000000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
+      PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                    p.total_units, p.column_major);
+      sched.init(pair);
+      bool ok = true;
+      while (ok && sched.valid()) {
+        const uint32_t w = sched.current_iter;
+        const uint32_t halves = sched.part >= 0 ? 1u : 2u;
+        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+          const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
+          const uint32_t s = static_cast<uint32_t>(phase % kWideStages);
+          const uint32_t par = static_cast<uint32_t>((phase / kWideStages) & 1u);
+          if (!pair_wait_or_abort(bar_loaded + 8u * s, par, abort_flag, peer_abort, limit,
+                                  kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after_sync();
+          const uint32_t a_addr = sA0 + s * kWideStageBytes;
+          const uint32_t b_addr = sB0 + s * kWideStageBytes;
+#pragma unroll
+          for (uint32_t h = 0; h < 2; ++h) {
+            if (h >= halves) break;
+            if (k == 0) {
+              // half h of the previous unit's accumulator has been read out by both epilogues
+              if (!pair_wait_or_abort(bar_tmem_empty + 8u * h, (w & 1u) ^ 1u, abort_flag,
+                                      peer_abort, limit, kRoleMma)) {
+                ok = false;
+                break;
+              }
+              tcgen05_fence_after_sync();
+            }
+#pragma unroll
+            for (uint32_t kk = 0; kk < kWideBK / kUmmaK; ++kk) {
+              const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+              const uint64_t b_desc = smem_desc_sw128(
+                  b_addr + 2u * h * kWideBChunkBytes + kk * kUmmaK * 128u, kWideBChunkBytes, 1024);
+              umma_f16_pair(tmem_base + h * kBN, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(bar_tmem_full, 0x3);
+        sched.next_tile();
+      }
+      umma_commit_pair_multicast(bar_drain, 0x1);
+      wait_bounded(bar_drain, 0, limit, kRoleDrain);
+    }
+    __syncwarp();
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const uint32_t q = warp - kFirstEpiWarp;
+    PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
+                                  p.total_units, p.column_major);
+    sched.init(pair);
+    uint32_t chunk = 0;
+    while (sched.valid()) {
+      const uint32_t w = sched.current_iter;
+      const bool got = pair_wait_or_abort(bar_tmem_full, w & 1u, abort_flag, peer_abort, limit,
+                                          kRoleEpilogue);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tcgen05_fence_after_sync();
+      const bool half = sched.part >= 0;
+      const uint32_t halves = half ? 1u : 2u;
+      const int32_t row0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM + q * 32u);
+      const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kWideBN + (half ? sched.part * kBN : 0);
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16);
+#pragma unroll 1
+      for (uint32_t h = 0; h < 2; ++h) {
+        if (h >= halves) {
+          tcgen05_fence_before_sync();
+          mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));   // unused half
+          continue;
+        }
+#pragma unroll 1
+        for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+          uint32_t v[64];
+          tmem_ld_32x32b_x64(t_row + h * kBN + j * kEpiN, v);
+          if (j == kBN / kEpiN - 1) {
+            // half h fully in registers: hand it back to the MMA before storing
+            tcgen05_fence_before_sync();
+            mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));
+          }
+          const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
+          epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
+                                   col0 + static_cast<int32_t>(h * kBN + j * kEpiN));
+        }
+      }
+      if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
+        int32_t* tr = p.trace + 5ull * sched.linear_idx;
+        tr[0] = static_cast<int32_t>(pair);
+        tr[1] = static_cast<int32_t>(w);
+        tr[2] = static_cast<int32_t>(sched.m_idx);
+        tr[3] = static_cast<int32_t>(sched.n_idx);
+        tr[4] = sched.part;
+      }
+      sched.next_tile();
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tcgen05_fence_before_sync();
+  cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
+  if (warp == 2) {
+    tcgen05_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tg

@@ -42,14 +42,14 @@ struct MxLaunch {
 };
 
 // kernel variants: one CTA per 128 x 256 tile, or a CTA pair (cta_group::2) per 256 x 256 tile
-enum Variant { kVariantSingle = 1, kVariantPair = 2 };
+enum Variant { kVariantSingle = 1, kVariantPair = 2, kVariantPairWide = 3 };
 
 // Sets the dynamic shared-memory limit of every GEMM instantiation on the current device and
 // returns how many CTA pairs of the pair kernels can be resident at once (*max_pairs: the
 // smaller of the dense and the MXFP8 pair kernel).
 cudaError_t prepare_gemm_kernels(int* max_pairs);
-// dtype 0 = fp16, 1 = bf16.  For the pair variant l.grid counts CTAs (even) and l.m_blocks
-// counts 256-row pair tiles.
+// dtype 0 = fp16, 1 = bf16.  For the pair variants l.grid counts CTAs (even) and l.m_blocks
+// counts 256-row pair tiles (l.n_blocks: 512-column tiles for kVariantPairWide).
 cudaError_t launch_gemm(int dtype, bool debug, int variant, const GemmLaunch& l,
                         cudaStream_t stream);
 // out_dtype 0 = fp16, 1 = bf16; variant kVariantSingle or kVariantPair (l.grid counts CTAs)

@@ -28,7 +28,7 @@ def nan_filled(M, N, dtype):
 
 # the kernel variants every parity test runs; "auto" is what tg_gemm_persistent (and the
 # benchmark) runs
-VARIANTS = ["single", "pair"]
+VARIANTS = ["single", "pair", "wide"]
 
 
 def run_gpu(a_cpu, b_cpu, dtype, stream=None, variant=None):

@@ -151,3 +151,12 @@ def test_group_width_option_rejections(lib):
     with pytest.raises(tg.TgError) as e:
         tg.tg_gemm_persistent_ex(16, 16, 16, 8, 8, 8, "bf16", stream=0, variant=1 << 24)
     assert e.value.code == tg.TG_ERR_ARG
+
+
+def test_mxfp8_rejects_the_dense_only_wide_variant(lib):
+    import persistent_warp_specialized_gb300 as tg
+
+    tg.load_library()
+    with pytest.raises(tg.TgError) as e:     # rejected before any CUDA call
+        tg.tg_gemm_mxfp8_ex(16, 16, 16, 16, 16, 256, 256, 128, "bf16", stream=0, variant="wide")
+    assert e.value.code == tg.TG_ERR_ARG

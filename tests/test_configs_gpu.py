@@ -36,8 +36,8 @@ def _inputs_and_oracle(name):
 def test_workload_matches_oracle(name, variant):
     w, a, b, ref = _inputs_and_oracle(name)
     if variant is None:
-        assert tg.tg_gemm_launch_shape(w.M, w.N, w.K)["variant"] in (tg.TG_VARIANT_SINGLE,
-                                                                     tg.TG_VARIANT_PAIR)
+        assert tg.tg_gemm_launch_shape(w.M, w.N, w.K)["variant"] in (
+            tg.TG_VARIANT_SINGLE, tg.TG_VARIANT_PAIR, tg.TG_VARIANT_PAIR_WIDE)
     got = run_gpu(a, b, w.dtype, variant=variant)
     assert_within_tolerance(got, ref, w.dtype, f"{name} {variant or 'auto'}")
     # beyond the gate: within the fp32 summation bound; ulp distances are reported only

@@ -97,9 +97,10 @@ def test_all_ones_give_k(dtype, K, variant):
 @pytest.mark.parametrize("plain", [False, True])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_split_tail_after_full_waves_is_bit_exact(variant, plain):
-    # 2560 x 2560: 200 single tiles (152 + a last wave of 48) or 100 pair tiles (76 + 24):
-    # the last wave runs as half-width units unless the plain page order is asked for
-    M, N, K = 2560, 2560, 448
+    # 2560 x 2560: 200 single tiles (152 + a last wave of 48) or 100 pair tiles (76 + 24);
+    # 5120 x 2560: 100 wide pair tiles (76 + 24).  The last wave runs as half-width units
+    # unless the plain page order is asked for
+    M, N, K = (5120, 2560, 448) if variant == "wide" else (2560, 2560, 448)
     shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
     assert (shape["units"] > shape["split_from"]) == (not plain)
     a, b = wl.small_int_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=11)
