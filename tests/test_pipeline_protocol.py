@@ -359,3 +359,96 @@ def test_mx_scales_arriving_on_loaded_are_caught():
     # some interleaving completes a phase of loaded[s] before the producer armed it
     failures = [run_mx_scales(4, 8, 40, seed, shared_loaded=True) for seed in range(150)]
     assert any(f is not None for f in failures)
+
+
+# ---------------------------------------------------------------- wide pair accumulator
+# The wide pair kernel (tg_gemm_pair_wide_kernel.cuh) has one accumulator made of two N-halves
+# (TMEM columns 0..255 and 256..511) in each CTA of the pair.  The MMA role (even CTA) writes
+# half h of unit w from its first k-block on, after waiting tmem_empty[h] with parity
+# (w & 1) ^ 1; after the unit it completes tmem_full in both CTAs.  Each CTA's epilogue waits
+# tmem_full with parity w & 1, reads the halves the unit uses and arrives on tmem_empty[h] of
+# the even CTA (count: both CTAs' epilogues); a half unit (one N-half) hands its unused half
+# back at once, so both barriers complete once per unit.
+
+
+def run_wide_accumulator(halves, k_blocks, seed, release_unused=True):
+    """halves[w] in {1, 2}: the N-halves unit w uses.  Returns None or the first violation."""
+    rng = random.Random(seed)
+    units = len(halves)
+    full = [Barrier(), Barrier()]                    # one per CTA, completed together
+    empty = [CountBarrier(2), CountBarrier(2)]       # per N-half, in the even CTA
+    acc = [[None, None], [None, None]]               # acc[cta][h] = [unit, k-blocks written, read?]
+    mma = {"w": 0, "k": 0, "h": 0}
+    epi = [{"w": 0, "h": 0, "waiting": True}, {"w": 0, "h": 0, "waiting": True}]
+    while any(e["w"] < units for e in epi):
+        moves = []
+        w, k, h = mma["w"], mma["k"], mma["h"]
+        if w < units:
+            if k > 0 or empty[h].passes((w & 1) ^ 1):
+                moves.append(("mma",))
+        for c in (0, 1):
+            e = epi[c]
+            if e["w"] >= units:
+                continue
+            if e["waiting"]:
+                if full[c].passes(e["w"] & 1):
+                    moves.append(("epi_start", c))
+            else:
+                moves.append(("epi_half", c))
+        if not moves:
+            return f"deadlock: mma {mma}, epilogues {epi}"
+        move = rng.choice(moves)
+        if move[0] == "mma":
+            for c in (0, 1):
+                cur = acc[c][h]
+                if k == 0:
+                    if cur is not None and not cur[2]:
+                        return f"unit {w} overwrote half {h} of CTA {c} before unit {cur[0]} was read"
+                    acc[c][h] = [w, 1, False]
+                else:
+                    if cur is None or cur[0] != w:
+                        return f"unit {w} accumulated into half {h} of CTA {c} owned by {cur}"
+                    cur[1] += 1
+            # next MMA step: halves in order inside a k-block, then the next k-block
+            if h + 1 < halves[w]:
+                mma["h"] = h + 1
+            else:
+                mma["h"] = 0
+                if k + 1 < k_blocks:
+                    mma["k"] = k + 1
+                else:
+                    full[0].complete()
+                    full[1].complete()
+                    mma.update(w=w + 1, k=0, h=0)
+        elif move[0] == "epi_start":
+            epi[move[1]]["waiting"] = False
+        else:
+            c = move[1]
+            e = epi[c]
+            hh = e["h"]
+            if hh < halves[e["w"]]:
+                cur = acc[c][hh]
+                if cur is None or cur[0] != e["w"] or cur[1] != k_blocks:
+                    return f"CTA {c} read half {hh} of unit {e['w']} as {cur}"
+                cur[2] = True
+                empty[hh].arrive()
+            elif release_unused:
+                empty[hh].arrive()
+            if hh == 1:
+                e.update(w=e["w"] + 1, h=0, waiting=True)
+            else:
+                e["h"] = 1
+    return None
+
+
+@pytest.mark.parametrize("halves", [[2], [2, 2, 2], [2, 2, 1], [1], [2, 1, 2, 1, 2], [1, 1, 2]])
+@pytest.mark.parametrize("k_blocks", [1, 2, 5])
+def test_wide_accumulator_protocol_holds(halves, k_blocks):
+    for seed in range(60):
+        assert run_wide_accumulator(halves, k_blocks, seed) is None
+
+
+def test_wide_half_unit_must_hand_back_its_unused_half():
+    # without the immediate hand-back, the unit after a half unit waits forever on half 1
+    results = [run_wide_accumulator([2, 1, 2], 2, seed, release_unused=False) for seed in range(20)]
+    assert all(r is not None and r.startswith("deadlock") for r in results)
