@@ -306,7 +306,9 @@ def workload_config(w):
             "accumulate": "fp32", "inputs": f"{w.dist}, seed {w.seed}",
             "l2": "inputs larger than L2 (no flush)" if 2 * (w.M * w.K + w.K * w.N) > 129e6
                   else "inputs fit in L2 (no flush; warm L2)",
-            "tile": "block_K 64; persistent: one scheduler worker per SM (single) or SM pair (pair)"}
+            "tile": "single 128x256 (block_K 64, 4 stages), pair 256x256 (block_K 128, 3 stages) or "
+                    "wide pair 256x512 (block_K 64, 4 stages), as config.launch says; persistent: one "
+                    "scheduler worker per SM (single) or SM pair (pair, wide pair)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm

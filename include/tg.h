@@ -175,11 +175,11 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
 
 /*
  * tg_gemm_launch_shape -- the persistent launch the library would use for an M x N x K
- * problem on the current device with ``variant`` (TG_VARIANT_*, optionally | TG_SCHEDULE_PLAIN;
- * AUTO is resolved).
+ * dense GEMM on the current device with ``variant`` (TG_VARIANT_*, optionally |
+ * TG_SCHEDULE_PLAIN; AUTO is resolved as tg_gemm_persistent resolves it).
  *   *variant_out: the concrete variant; *tile_m, *tile_n: the output tile of one scheduler
- *   worker; *m_tiles, *n_tiles: the tile grid; *workers: scheduler workers (CTAs for SINGLE,
- *   CTA pairs for PAIR); *ctas: CTAs launched; *split_from, *units: the tail split (units
+ *   worker (256 x 512 for PAIR_WIDE); *m_tiles, *n_tiles: the tile grid; *workers: scheduler
+ *   workers (CTAs for SINGLE, CTA pairs for PAIR and PAIR_WIDE); *ctas: CTAs launched; *split_from, *units: the tail split (units
  *   below split_from are whole tiles; split_from == units: no split).  Any pointer may be NULL.
  * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
  */
