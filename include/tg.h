@@ -92,9 +92,11 @@ enum {
  *   A_dev [M, K], B_dev [K, N], C_dev [M, N]; all of type ``dtype`` (TG_F16 or TG_BF16).
  *   M, N, K >= 0 and < 2^31.  N % 8 == 0 and K % 8 == 0.  All three pointers 16-byte aligned.
  *   C must not overlap A or B.  M == 0 or N == 0: nothing is done.  K == 0: C is zero-filled.
- * One persistent CTA per SM (at most the number of output tiles) walks 128 x 256 output tiles
- * in grouped order (group 8); see tg_tile_schedule.  Partial edge tiles in M and N and a
- * partial last k-block are handled inside the kernel (zero-filled loads, clipped stores).
+ * Persistent kernels walk the output tiles in grouped order (group 8; see tg_tile_schedule):
+ * one CTA per SM on 128 x 256 tiles, or one CTA pair per two SMs on 256 x 256 or 256 x 512
+ * tiles, chosen as TG_VARIANT_AUTO describes at tg_gemm_persistent_ex.  Partial edge tiles in
+ * M and N and a partial last k-block are handled inside the kernel (zero-filled loads,
+ * clipped stores).
  */
 int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
                        int64_t M, int64_t N, int64_t K, int dtype, void* stream);
