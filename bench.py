@@ -668,6 +668,10 @@ def main(argv=None):
     from persistent_warp_specialized_gb300 import workloads as wl
 
     if args.workload in wl.MX_WORKLOADS:
+        if args.variant == "wide":
+            print("--variant wide is a dense-GEMM kernel; the MXFP8 GEMM has single and pair",
+                  file=sys.stderr)
+            return 2
         return run_reference_mx(args) if args.impl == "reference" else run_tg_mx(args)
     if args.impl == "reference":
         return run_reference(args)

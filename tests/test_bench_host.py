@@ -147,3 +147,11 @@ def test_reference_block_side_bounds_one_step():
     dt = time.perf_counter() - t0
     assert 0.1 <= dt <= 0.9
     assert bench.block_side(run, 100, 5.0) == 100     # never beyond the matrix
+
+
+def test_mxfp8_workload_rejects_the_dense_only_variant():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "mxfp8_512",
+                        "--variant", "wide", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 2 and r.stdout.strip() == ""
+    assert "dense" in r.stderr
