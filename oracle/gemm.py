@@ -12,6 +12,19 @@ its fp32 additions, so the oracle is the plain definition: every product of two
 binary16/bfloat16 values is exact in binary64 (at most 22 significant bits), the sum is
 accumulated in binary64 by numpy's float64 matrix product (a library step), and the
 result is rounded once to the output type.
+
+Two statements of the same binary64 sum are kept:
+* ``gemm_f64_by_k`` is the definition written out: K rank-1 updates C += A[:, k] B[k, :],
+  taken in k order with elementwise binary64 multiplies and adds (the i and j loops of the
+  triple loop are numpy's elementwise loops; no library contraction).  It is slow (K passes
+  over C) and serves as the reference the fast form is pinned against.
+* ``gemm_f64`` is the same sum by numpy's float64 matrix product (BLAS): blocked, threaded
+  and in its own order.  Every binary64 sum of the same terms lies within
+  gamma_K * sum_k |A[i,k] B[k,j]| of the exact sum (gamma_K = K u / (1 - K u), u = 2^-53),
+  so the two differ by at most twice that, far below half an ulp of the 16-bit output for
+  all but outputs within that distance of a rounding boundary.  The pins compare them at
+  sizes where the BLAS takes its blocked, multithreaded path, and compare the BLAS with
+  exact integer arithmetic there.
 """
 
 import numpy as np
@@ -26,6 +39,18 @@ def gemm_f64(a_bits, b_bits, in_fmt):
     if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[0]:
         raise ValueError(f"shapes {a.shape} x {b.shape} do not contract")
     return a @ b
+
+
+def gemm_f64_by_k(a_bits, b_bits, in_fmt):
+    """The same sum without a library contraction: K rank-1 updates in k order, binary64."""
+    a = formats.decode(a_bits, in_fmt)
+    b = formats.decode(b_bits, in_fmt)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shapes {a.shape} x {b.shape} do not contract")
+    c = np.zeros((a.shape[0], b.shape[1]), dtype=np.float64)
+    for k in range(a.shape[1]):
+        c += np.multiply.outer(a[:, k], b[k, :])
+    return c
 
 
 def gemm_ref(a_bits, b_bits, in_fmt, out_fmt=None):

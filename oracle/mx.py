@@ -22,6 +22,9 @@ A's); ``sa`` [M, K/32] and ``sb`` [N, K/32] hold E8M0 byte patterns.  Every prod
 E4M3 values has at most 8 significant bits and the scales are powers of two within
 2^+-254, so every scaled product is exact in binary64; the sum is binary64 (numpy's
 float64 matrix product, a library step); the result is rounded once to the output type.
+``gemm_mxfp8_f64_by_k`` states the same sum without a library contraction (K rank-1
+updates in k order); the pins compare the two, and the library product with exact integer
+arithmetic, at sizes where the library blocks and threads.
 """
 
 import numpy as np
@@ -65,6 +68,18 @@ def gemm_mxfp8_f64(a_bits, sa_bits, b_bits, sb_bits):
     if a.shape[1] != b.shape[1]:
         raise ValueError(f"K of A ({a.shape[1]}) and B ({b.shape[1]}) differ")
     return a @ b.T
+
+
+def gemm_mxfp8_f64_by_k(a_bits, sa_bits, b_bits, sb_bits):
+    """The same sum as K rank-1 updates of the scaled operands in k order, binary64."""
+    a = scaled(a_bits, sa_bits)
+    b = scaled(b_bits, sb_bits)
+    if a.shape[1] != b.shape[1]:
+        raise ValueError(f"K of A ({a.shape[1]}) and B ({b.shape[1]}) differ")
+    c = np.zeros((a.shape[0], b.shape[0]), dtype=np.float64)
+    for k in range(a.shape[1]):
+        c += np.multiply.outer(a[:, k], b[:, k])
+    return c
 
 
 def gemm_mxfp8_ref(a_bits, sa_bits, b_bits, sb_bits, out_fmt="bf16"):

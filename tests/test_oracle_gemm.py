@@ -4,9 +4,10 @@ A plausible mistake in the oracle -- a transposed operand, a dropped or repeated
 a wrong decode or rounding -- fails at least one of these:
 * all-ones matrices give C = K exactly;
 * an identity factor reproduces the other operand bit for bit (A = I gives B, B = I gives A);
-* on tiny non-square shapes every entry equals the exact rational sum computed with
-  Python's ``fractions`` (products and sums done without rounding), to within the
-  binary64 summation error bound, and the rounded result equals the correctly rounded
+* on tiny non-square shapes every entry of both binary64 statements of the sum (the library
+  product and the loop over k) equals the exact rational sum computed with Python's
+  ``fractions`` (products and sums done without rounding), to within the binary64
+  summation error bound, and the rounded result equals the correctly rounded
   exact sum whenever the exact sum is not within that bound of a rounding boundary;
 * integer-valued inputs give exactly Python's integer matrix product.
 """
@@ -69,14 +70,16 @@ def test_tiny_shapes_against_exact_rationals(fmt, shape):
     a = _bits_of(rng.uniform(-1, 1, (M, K)), fmt)
     b = _bits_of(rng.uniform(-1, 1, (K, N)), fmt)
     c64 = gemm.gemm_f64(a, b, fmt)
-    assert c64.shape == (M, N)
+    c64_by_k = gemm.gemm_f64_by_k(a, b, fmt)
+    assert c64.shape == (M, N) and c64_by_k.shape == (M, N)
     exact, absum = _exact(a, b, fmt)
     gamma = K * 2.0 ** -53 / (1 - K * 2.0 ** -53)
     cref = gemm.gemm_ref(a, b, fmt)
     for i in range(M):
         for j in range(N):
-            err = abs(Fraction(float(c64[i, j])) - exact[i][j])
-            assert err <= Fraction(gamma * absum[i, j]) + Fraction(1, 1 << 1074)
+            for c in (c64, c64_by_k):        # the library sum and the loop over k
+                err = abs(Fraction(float(c[i, j])) - exact[i][j])
+                assert err <= Fraction(gamma * absum[i, j]) + Fraction(1, 1 << 1074)
             # the rounded result: round the (binary64-nearest) exact value once
             nearest = float(exact[i][j])
             want = formats.round_rne(np.array([nearest]), fmt)[0]
@@ -118,3 +121,5 @@ def test_shape_mismatch_is_rejected():
     b = np.zeros((5, 2), np.uint16)
     with pytest.raises(ValueError):
         gemm.gemm_f64(a, b, "f16")
+    with pytest.raises(ValueError):
+        gemm.gemm_f64_by_k(a, b, "f16")
