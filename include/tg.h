@@ -155,8 +155,9 @@ int tg_tile_schedule_ex(int m_blocks, int n_blocks, int num_sms, int group, int 
  *   it calls no allocation routine.
  *   Arguments, flags, rows and return value: as tg_tile_schedule_ex.  A call with more than
  *   TG_SCHEDULE_NOALLOC_MAX_UNITS units returns TG_ERR_ARG before it touches the device.
- *   The first call on a device looks up the array's address there (with that device current):
- *   make that first call before any stream capture.  All calls on a device share the one array,
+ *   Every call looks up the array's address in the current device's context (the first call
+ *   on a device also loads the library's device image there): make that first call before
+ *   any stream capture.  All calls on a device share the one array,
  *   so calls that overlapped on the GPU would race; each call therefore holds a process-wide
  *   lock from its launch until its rows are on the host, and returns only then (legacy default
  *   stream).  Nothing needs clearing between calls: every row copied back is written by the

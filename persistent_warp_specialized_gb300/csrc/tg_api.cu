@@ -445,14 +445,15 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
 
 // Scratch of tg_tile_schedule_noalloc: TG_SCHEDULE_NOALLOC_MAX_UNITS rows of 5 int32 in the
 // library's device image, so that call needs no allocation.  In host code the name stands for a
-// host-side shadow, not a device address: the device address is looked up once per device with
-// cudaGetSymbolAddress and passed to the scheduler kernel.
+// host-side shadow, not a device address: every call looks the device address up with
+// cudaGetSymbolAddress on the current device and passes it to the scheduler kernel.  The
+// address is not cached, because a context torn down and created again (cudaDeviceReset) loads
+// the image anew, possibly elsewhere.
 static __device__ __align__(256) int32_t g_schedule_scratch[5 * TG_SCHEDULE_NOALLOC_MAX_UNITS];
 
 namespace {
 
-int32_t* g_schedule_scratch_dev[kMaxDevices];   // per device: address of g_schedule_scratch
-std::mutex g_schedule_scratch_mu;               // one call at a time uses the array
+std::mutex g_schedule_scratch_mu;   // one call at a time uses the array
 
 }  // namespace
 
@@ -633,18 +634,10 @@ int tg_tile_schedule_noalloc(int m_blocks, int n_blocks, int num_sms, int group,
                 "tg_tile_schedule_noalloc: %u units exceed its fixed scratch of %d units "
                 "(use tg_tile_schedule_ex)",
                 units, TG_SCHEDULE_NOALLOC_MAX_UNITS);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
-  if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_CUDA, "device ordinal %d unsupported", dev);
   std::lock_guard<std::mutex> lock(g_schedule_scratch_mu);
-  int32_t*& scratch = g_schedule_scratch_dev[dev];
-  if (scratch == nullptr) {
-    int32_t* ptr = nullptr;
-    e = cudaGetSymbolAddress((void**)&ptr, g_schedule_scratch);
-    if (e != cudaSuccess) return fail_cuda("address of the schedule scratch", e);
-    scratch = ptr;
-  }
+  int32_t* scratch = nullptr;   // the array's address in the current device's context
+  cudaError_t e = cudaGetSymbolAddress((void**)&scratch, g_schedule_scratch);
+  if (e != cudaSuccess) return fail_cuda("address of the schedule scratch", e);
   e = tg::launch_tile_schedule(uint32_t(m_blocks), uint32_t(n_blocks), uint32_t(num_sms),
                                uint32_t(group), first, units,
                                (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u, scratch, nullptr);

@@ -3,13 +3,15 @@
 tg_tile_schedule_ex stages its rows in a device buffer it allocates and frees inside the call.
 Callers whose device memory is all owned by their own pool allocator, or that must not stall
 on cudaFree (which waits for the whole device), use tg_tile_schedule_noalloc instead: it
-stages the rows in a fixed array in the library's device image.  Both must return the same
-rows.  The file is named so that pytest collects it last.
+stages the rows in a fixed array in the library's device image.  Its rows must equal the
+oracle's enumeration of the same traversal (and therefore the allocating call's).  The file is
+named so that pytest collects it last.
 """
 
 import pytest
 
 import persistent_warp_specialized_gb300 as tg
+from oracle import schedule
 
 from gpu_helpers import ensure_library
 
@@ -26,11 +28,13 @@ def test_noalloc_schedule_equals_the_allocating_one_on_consecutive_calls():
         (16, 28, 76, 8, False, False),      # 4096 x 7168 in pair tiles, no split
     ]
     for m, n, sms, group, split, cm in cases:
+        want = schedule.enumerate_units(m, n, sms, group, split_tail=split, column_major=cm)
         for _ in range(2):
             got = tg.tg_tile_schedule_noalloc(m, n, sms, group, split_tail=split,
                                               column_major=cm)
-            want = tg.tg_tile_schedule_ex(m, n, sms, group, split_tail=split, column_major=cm)
             assert got == want, (m, n, sms, group, split, cm)
+            assert got == tg.tg_tile_schedule_ex(m, n, sms, group, split_tail=split,
+                                                 column_major=cm)
 
 
 @pytest.mark.gpu
@@ -40,7 +44,7 @@ def test_noalloc_schedule_at_its_maximum_size():
     assert m * n == tg.TG_SCHEDULE_NOALLOC_MAX_UNITS
     got = tg.tg_tile_schedule_noalloc(m, n, 152, 8, split_tail=False)
     assert len(got) == m * n
-    assert got == tg.tg_tile_schedule_ex(m, n, 152, 8, split_tail=False)
+    assert got == schedule.enumerate_units(m, n, 152, 8, split_tail=False)
 
 
 def test_noalloc_schedule_rejects_sizes_beyond_its_scratch():
