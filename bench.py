@@ -15,7 +15,18 @@ copied in and C copied out every step; consecutive steps alternate between two s
 their own device buffers, so one step's copies overlap the other's GEMM), ``roofline`` (tensor-bound: achieved TFLOP/s over
 the measured cuBLAS bf16 peak of this GPU type), ``clocks`` (nvidia-smi sampled during the
 timed region) and ``cpu_baseline`` (the CPU oracle timed on a bounded row slab of the same
-workload, which also checks the GPU's rows of that slab).
+workload, which also checks the GPU's rows of that slab).  ``pct_of_dense_peak`` quotes the
+value against the one stated dense bf16 peak (``dense_peak``: 2.5 PFLOP/s, with its source).
+
+With the 8192^3 workload two more records follow the headline:
+* ``sustained``: back-to-back launches for ``--sustained-seconds`` (3 s) with clocks sampled,
+  the rate the kernel holds at the GPU's power limit;
+* ``per_config``: every workload of the metric (256^3 and 1024^3 fp16, 4096^3 and 8192^3
+  bf16, 4000 x 7000 x 2048 bf16) and the block-scaled MXFP8 GEMM at 8192^3, each timed as the
+  pages' benchmark times the kernel (50 warm-up and 50 timed launches), here with L2 flushed
+  before every timed launch and CUDA events around each; with the kernel the library picked,
+  compulsory DRAM GB/s, the CPU oracle's rate over the whole C on the host cores, and the gate
+  checked on every output.
 
 ``--impl reference`` times the CPU oracle instead (there is no other implementation of this
 path to run); under torchrun only rank 0 runs it.
@@ -39,7 +50,12 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (2MNK/t) at 4096³/8192³ bf16 on 1 GB300; % of dense tensor peak"
 UNIT = "TFLOP/s"
-NOMINAL_DENSE_BF16_TFLOPS = 2250.0       # GB300 dense bf16/fp16, no sparsity
+# The one dense bf16/fp16 tensor peak "% of dense tensor peak" is quoted against: NVIDIA's GB300
+# NVL72 datasheet gives 360 PFLOP/s FP16/BF16 for 72 GPUs with 2:4 sparsity, i.e. 2.5 PFLOP/s
+# dense per GPU (152 SMs x 8192 flop/clk reach it at 2.0 GHz).
+DENSE_PEAK_TFLOPS = 2500.0
+DENSE_PEAK_SOURCE = ("NVIDIA GB300 NVL72 datasheet: FP16/BF16 tensor 360 PFLOP/s per 72 GPUs "
+                     "with 2:4 sparsity = 2.5 PFLOP/s dense per GPU")
 DENSE_FLOP_PER_CLK_PER_SM = 8192         # derived: one 128x256x16 MMA per 128 cycles
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILES = os.path.join(ROOT, "profiles")
@@ -55,10 +71,17 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="gemm_8192_bf16")
     ap.add_argument("--variant", choices=["auto", "single", "pair", "wide"], default="auto",
                     help="kernel variant (auto: the library's choice, as tg_gemm_persistent)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="end-to-end steps through the host-buffer entry point (0: leave out)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload records (every workload of the metric, each timed "
+                         "with L2 flushed before every launch and checked against the oracle)")
+    ap.add_argument("--sustained-seconds", type=float, default=3.0,
+                    help="length of the sustained back-to-back run of the headline workload "
+                         "(0: skip)")
     return ap.parse_args(argv)
 
 
@@ -373,6 +396,190 @@ def time_e2e(make_step, e_steps, dev, world, lanes=2):
     return max_over_ranks(start.elapsed_time(end) / e_steps, dev if world > 1 else None)
 
 
+L2_FLUSH_BYTES = 256 << 20     # written before every per-config launch: twice the 129 MB L2
+PER_CONFIG_WARMUP = 50         # the pages' benchmark: do_bench(..., _n_warmup=50, _n_repeat=50)
+PER_CONFIG_REPEAT = 50
+
+
+def time_flushed(step, dev, flush, warmup=PER_CONFIG_WARMUP, repeat=PER_CONFIG_REPEAT):
+    """Device milliseconds of ``step`` per launch: ``warmup`` untimed launches, then ``repeat``
+    launches, each after a write of a buffer twice the size of L2 and between its own pair of
+    CUDA events on the launching stream.  Returns (median, best, mean of the back-to-back
+    launches of the warm-up's second half, which run with a warm L2)."""
+    import torch
+
+    stream = torch.cuda.current_stream(dev)
+    half = max(1, warmup // 2)
+    for _ in range(warmup - half):
+        step()
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(half):
+        step()
+    b1.record(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(repeat)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(repeat)]
+    for i in range(repeat):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sorted(a.elapsed_time(b) for a, b in zip(starts, ends))
+    return statistics.median(ms), ms[0], b0.elapsed_time(b1) / half
+
+
+def oracle_full(w, a_cpu, b_cpu):
+    """The oracle's whole C for ``w`` on the host cores: (bits, seconds)."""
+    from oracle import gemm as ogemm
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    a_bits, b_bits = wl.bits(a_cpu), wl.bits(b_cpu)
+    t0 = time.perf_counter()
+    ref = ogemm.gemm_ref(a_bits, b_bits, w.dtype)
+    return ref, time.perf_counter() - t0
+
+
+def gate(got_bits, ref_bits, fmt):
+    """(within |C - C_ref| <= 5e-3 + 1e-2 |C_ref| everywhere and finite, max |C - C_ref|)."""
+    import numpy as np
+
+    from oracle import formats
+
+    got = formats.decode(got_bits, fmt)
+    want = formats.decode(ref_bits, fmt)
+    err = np.abs(got - want)
+    ok = bool(np.isfinite(got).all() and (err <= 5e-3 + 1e-2 * np.abs(want)).all())
+    return ok, float(err.max())
+
+
+def per_config_records(dev, peaks, headline, cores):
+    """One record per workload of the metric: device TFLOP/s (median and best of 50 launches
+    after 50 warm-up, L2 flushed before each), the kernel the library picked, compulsory DRAM
+    GB/s, the CPU oracle's TFLOP/s on the host cores over the whole C, and whether every
+    output is within the gate.  ``headline``: (workload, a_cpu, b_cpu, a, b, c, ref, secs) of
+    the workload already on the device and checked, so it is neither drawn nor computed twice."""
+    import torch
+
+    import persistent_warp_specialized_gb300 as tg
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    records = []
+    for w in wl.WORKLOADS.values():
+        if headline is not None and w.name == headline[0].name:
+            _, a_cpu, b_cpu, a, b, c, ref, secs = headline
+        else:
+            a_cpu, b_cpu = wl.workload_inputs(w)
+            a, b = a_cpu.to(dev), b_cpu.to(dev)
+            c = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.dtype], device=dev)
+            ref = secs = None
+
+        def step(a=a, b=b, c=c, w=w):
+            tg.tg_gemm_persistent(a, b, c, w.M, w.N, w.K, w.dtype)
+
+        med, best, warm = time_flushed(step, dev, flush)
+        tg.tg_device_status()
+        if ref is None:
+            ref, secs = oracle_full(w, a_cpu, b_cpu)
+        ok, max_err = gate(wl.bits(c.cpu()), ref, w.dtype)
+        launch = tg.tg_gemm_launch_shape(w.M, w.N, w.K)
+        compulsory = 2 * (w.M * w.K + w.K * w.N + w.M * w.N)
+        tflops = w.flops / (med * 1e-3) / 1e12
+        records.append({
+            "workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
+            "inputs": f"{w.dist}, seed {w.seed}",
+            "kernel": KERNEL_NAMES[launch["variant"]], "launch": launch,
+            "tflops": tflops, "tflops_best": w.flops / (best * 1e-3) / 1e12,
+            "ms_median": med, "ms_best": best,
+            "frac_of_dense_peak": tflops / DENSE_PEAK_TFLOPS,
+            "tflops_back_to_back_warm_l2": w.flops / (warm * 1e-3) / 1e12,
+            "compulsory_bytes": compulsory,
+            "hbm_gbs": compulsory / (med * 1e-3) / 1e9,
+            "hbm_frac": compulsory / (med * 1e-3) / 1e9 / hbm,
+            "cpu_oracle_tflops": w.flops / secs / 1e12, "cpu_oracle_s": secs,
+            "cpu_oracle_cores": cores,
+            "within_tolerance": ok, "max_abs_err": max_err,
+            "timing": f"{PER_CONFIG_WARMUP} warm-up + {PER_CONFIG_REPEAT} timed launches, each "
+                      f"after a {L2_FLUSH_BYTES >> 20} MiB write (L2 flushed), CUDA events per "
+                      f"launch; median",
+        })
+        del a, b, c
+    del flush
+    torch.cuda.empty_cache()
+    return records
+
+
+def mx_per_config_record(dev, peaks, cores, rows=1024):
+    """The block-scaled MXFP8 workload at 8192^3: the GEMM kernel alone and the whole step
+    (both scale packs + the GEMM), each timed like the dense records, plus the oracle on
+    ``rows`` rows of C (its time scaled to TFLOP/s) and the gate on those rows."""
+    import torch
+
+    import persistent_warp_specialized_gb300 as tg
+    from oracle import mx
+    from persistent_warp_specialized_gb300 import workloads as wl
+
+    M, N, K, seed = wl.MX_WORKLOADS["mxfp8_8192"]
+    host = wl.make_mx_inputs(M, N, K, seed)
+    a, sa, b, sb = (t.to(dev) for t in host)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    sa_p = torch.empty(tg.tg_mxfp8_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    sb_p = torch.empty(tg.tg_mxfp8_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flops = 2.0 * M * N * K
+
+    def gemm():
+        tg.tg_gemm_mxfp8(a, sa_p, b, sb_p, c, M, N, K, "bf16")
+
+    def step():
+        tg.tg_mxfp8_pack_scales(sa, sa_p, M, K)
+        tg.tg_mxfp8_pack_scales(sb, sb_p, N, K)
+        gemm()
+
+    step_med, _, _ = time_flushed(step, dev, flush)
+    med, best, warm = time_flushed(gemm, dev, flush)
+    tg.tg_device_status()
+    an, san, bn, sbn = (t.numpy() for t in host)
+    t0 = time.perf_counter()
+    ref = mx.gemm_mxfp8_ref(an[:rows], san[:rows], bn, sbn, "bf16")
+    secs = time.perf_counter() - t0
+    ok, max_err = gate(wl.bits(c[:rows].cpu()), ref, "bf16")
+    launch = tg.tg_gemm_launch_shape(M, N, K, "pair")
+    tflops = flops / (med * 1e-3) / 1e12
+    compulsory = M * K + N * K + (M * K + N * K) // 32 + 2 * M * N   # GEMM: A, B, scales, C
+    rec = {
+        "workload": "mxfp8_8192", "M": M, "N": N, "K": K, "dtype": "e4m3 (e8m0 scales per 32), bf16 out",
+        "inputs": f"MX-quantized N(0,1) / N(0,1/K) draws, seed {seed}",
+        "kernel": "gemm_mxfp8_pair_ws", "launch": launch,
+        "tflops": tflops, "tflops_best": flops / (best * 1e-3) / 1e12, "ms_median": med,
+        "tflops_step_with_packs": flops / (step_med * 1e-3) / 1e12,
+        "frac_of_dense_peak": tflops / (2 * DENSE_PEAK_TFLOPS),
+        "tflops_back_to_back_warm_l2": flops / (warm * 1e-3) / 1e12,
+        "compulsory_bytes": compulsory, "hbm_gbs": compulsory / (med * 1e-3) / 1e9,
+        "hbm_frac": compulsory / (med * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0)),
+        "cpu_oracle_tflops": 2.0 * rows * N * K / secs / 1e12, "cpu_oracle_s": secs,
+        "cpu_oracle_cores": cores, "cpu_oracle_sample": f"rows [0, {rows}) of C",
+        "within_tolerance": ok, "max_abs_err": max_err, "checked_rows": rows,
+        "timing": "as the dense records; tflops is the GEMM kernel alone",
+    }
+    del a, sa, b, sb, c, sa_p, sb_p, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def sustained_record(step, flops, ms_estimate, seconds, dev, stream, world):
+    """Back-to-back launches of the headline step for about ``seconds`` with clocks sampled:
+    what the kernel holds once the GPU sits at its power limit."""
+    n = max(10, int(seconds / max(ms_estimate * 1e-3, 1e-6)))
+    ms_local, ms, clocks = timed_region(step, n, 3, dev, stream, world)
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"launches": n, "seconds": n * ms * 1e-3, "ms_per_launch": ms, "tflops": tflops,
+            "frac_of_dense_peak": tflops / DENSE_PEAK_TFLOPS, "clocks": clocks}
+
+
 def run_tg(args):
     import torch
 
@@ -420,13 +627,15 @@ def run_tg(args):
             tg.tg_gemm_persistent_host(a_h, b_h, c_h, a2, b2, c2, w.M, w.N, w.K, w.dtype, st)
         return e2e_step
 
-    e_ms = time_e2e(make_e2e_step, max(1, args.e2e_steps), dev, world)
-    tg.tg_device_status(stream)
-    h2d = 2 * (w.M * w.K + w.K * w.N)
-    d2h = 2 * w.M * w.N
-    e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-           "streams": 2, "api": "tg_gemm_persistent_host"}
+    e2e = None                       # --e2e-steps 0: profiling runs leave the e2e leg out
+    if args.e2e_steps > 0:
+        e_ms = time_e2e(make_e2e_step, args.e2e_steps, dev, world)
+        tg.tg_device_status(stream)
+        h2d = 2 * (w.M * w.K + w.K * w.N)
+        d2h = 2 * w.M * w.N
+        e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "streams": 2, "api": "tg_gemm_persistent_host"}
 
     launch = tg.tg_gemm_launch_shape(w.M, w.N, w.K, args.variant)
     kernel = KERNEL_NAMES[launch["variant"]]
@@ -442,8 +651,8 @@ def run_tg(args):
                 "traffic": profile_traffic(kernel, w.name),
                 "peak_source": f"{peak_src} ({peak_note}, cuBLAS torch.matmul)",
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                "frac_of_nominal_dense": achieved / NOMINAL_DENSE_BF16_TFLOPS,
-                "nominal_dense_tflops": NOMINAL_DENSE_BF16_TFLOPS}
+                "frac_of_dense_peak": achieved / DENSE_PEAK_TFLOPS,
+                "dense_peak_tflops": DENSE_PEAK_TFLOPS}
     if clocks and clocks.get("sm_mhz"):
         clk_peak = sms * DENSE_FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak
@@ -456,27 +665,40 @@ def run_tg(args):
         "config": dict(workload_config(w), sms=sms,
                        launch=launch),
         "gpu_launches": steps, "e2e": e2e, "roofline": roofline, "clocks": clocks,
+        "pct_of_dense_peak": 100.0 * value / world / DENSE_PEAK_TFLOPS,
+        "dense_peak": {"tflops": DENSE_PEAK_TFLOPS, "source": DENSE_PEAK_SOURCE},
     }
 
+    headline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import numpy as np
-
-        from oracle import formats
-
         a_bits, b_bits = wl.bits(a_cpu), wl.bits(b_cpu)
         rows, dt, ref = timed_oracle_sample(lambda r: oracle_slab(a_bits, b_bits, w.dtype, r),
                                             w.M, args.cpu_seconds)
-        got = formats.decode(wl.bits(c[:rows].cpu()), w.dtype)
-        want = formats.decode(ref, w.dtype)
-        err = np.abs(got - want)
-        ok = bool(np.isfinite(got).all() and (err <= 5e-3 + 1e-2 * np.abs(want)).all())
+        ok, max_err = gate(wl.bits(c[:rows].cpu()), ref, w.dtype)
+        cores = blas_threads()
         line["cpu_baseline"] = {
-            "value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": UNIT, "cores": blas_threads(),
+            "value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"rows [0, {rows}) of C ({rows} x {w.N} outputs, K={w.K}): decode, "
                       f"binary64 product (numpy/OpenBLAS), round to {w.dtype}; {dt:.1f} s"}
         line["parity_sample"] = {"rows": rows, "cols": w.N, "within_tolerance": ok,
-                                 "max_abs_err": float(err.max())}
+                                 "max_abs_err": max_err}
+        if rows == w.M and args.variant == "auto":
+            headline = (w, a_cpu, b_cpu, a, b, c, ref, dt)
+
+    if args.sustained_seconds > 0 and w.name == "gemm_8192_bf16":
+        line["sustained"] = sustained_record(step, w.flops, ms, args.sustained_seconds, dev,
+                                             stream, world)
+        line["sustained"]["tflops"] *= world
+
+    if rank == 0 and world == 1 and not args.no_per_config and not args.no_cpu_baseline:
+        cores = blas_threads()
+        del a_h, b_h
+        line["per_config"] = per_config_records(dev, peaks, headline, cores)
+        headline = None
+        del a, b, c
+        torch.cuda.empty_cache()
+        line["per_config"].append(mx_per_config_record(dev, peaks, cores))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -626,8 +848,8 @@ def run_tg_mx(args):
                 "traffic": profile_traffic(kernel, f"{M}_mxfp8"),
                 "peak_source": f"{peak_src}: bf16 burst peak x 2 (the nominal dense fp8 / bf16 "
                                f"ratio, 4.5 / 2.25 PFLOP/s)",
-                "frac_of_nominal_dense": achieved / (2 * NOMINAL_DENSE_BF16_TFLOPS),
-                "nominal_dense_tflops": 2 * NOMINAL_DENSE_BF16_TFLOPS}
+                "frac_of_dense_peak": achieved / (2 * DENSE_PEAK_TFLOPS),
+                "dense_peak_tflops": 2 * DENSE_PEAK_TFLOPS}
     line = {
         "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
