@@ -847,7 +847,7 @@ def run_tg_mx(args):
                 "kernel_ms": gemm_ms,
                 "traffic": profile_traffic(kernel, f"{M}_mxfp8"),
                 "peak_source": f"{peak_src}: bf16 burst peak x 2 (the nominal dense fp8 / bf16 "
-                               f"ratio, 4.5 / 2.25 PFLOP/s)",
+                               f"ratio, 2)",
                 "frac_of_dense_peak": achieved / (2 * DENSE_PEAK_TFLOPS),
                 "dense_peak_tflops": 2 * DENSE_PEAK_TFLOPS}
     line = {
