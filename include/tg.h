@@ -178,17 +178,22 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
 
 /*
  * tg_gemm_launch_shape -- the persistent launch the library would use for an M x N x K
- * dense GEMM on the current device with ``variant`` (TG_VARIANT_*, optionally |
- * TG_SCHEDULE_PLAIN; AUTO is resolved as tg_gemm_persistent resolves it).
+ * dense GEMM on the current device with ``variant`` (TG_VARIANT_* with any TG_SCHEDULE_* flags;
+ * AUTO is resolved as tg_gemm_persistent resolves it).
  *   *variant_out: the concrete variant; *tile_m, *tile_n: the output tile of one scheduler
  *   worker (256 x 512 for PAIR_WIDE); *m_tiles, *n_tiles: the tile grid; *workers: scheduler
- *   workers (CTAs for SINGLE, CTA pairs for PAIR and PAIR_WIDE); *ctas: CTAs launched; *split_from, *units: the tail split (units
- *   below split_from are whole tiles; split_from == units: no split).  Any pointer may be NULL.
+ *   workers (CTAs for SINGLE, CTA pairs for PAIR and PAIR_WIDE); *ctas: CTAs launched;
+ *   *split_from, *units: the tail split (units below split_from are whole tiles;
+ *   split_from == units: no split); *group, *column_major: the traversal (the grouped order's
+ *   width and whether it runs along M first).  With TG_VARIANT_AUTO and no TG_SCHEDULE_PLAIN,
+ *   TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP flag, the library also picks the traversal:
+ *   whole rows of tiles when all of B fits in half of the L2 (64 MiB), whole columns when only
+ *   A does, else groups of 8 in row order.  Any pointer may be NULL.
  * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
  */
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
-                         int* ctas, int* split_from, int* units);
+                         int* ctas, int* split_from, int* units, int* group, int* column_major);
 
 /*
  * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
@@ -198,9 +203,12 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
  *     stored unit u saw them (worker = CTA, or CTA pair) -- evidence that the kernel followed
  *     the schedule of tg_tile_schedule_ex.
  *   watchdog_ns: limit for every wait inside the kernel (0 = the default of about 4 s).
- *   inject_skip_phase: -1 for none; otherwise CTA 0's producer never arms or fills that
- *     pipeline phase, so the MMA role's wait on it cannot complete: the watchdog must fire, every
- *     role must stop, and the call must return TG_ERR_TIMEOUT with the context intact.
+ *   inject_skip_phase: -1 for none; otherwise cta * 2^32 + phase: the producer of CTA ``cta``
+ *     (0 when inject_skip_phase < 2^32) never arms or fills that pipeline phase, so the MMA
+ *     role's wait on it cannot complete: the watchdog must fire, every role must stop, and the
+ *     call must return TG_ERR_TIMEOUT with the context intact.  In the CTA-pair kernels CTA 0 is
+ *     the even CTA of pair 0 (the other CTA of the pair still fills the phase) and CTA 1 the odd
+ *     one (the even CTA has armed the phase for both).
  * Synchronises ``stream``.  Returns TG_OK, TG_ERR_TIMEOUT or another error.
  */
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev,

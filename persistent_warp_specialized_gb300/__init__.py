@@ -92,7 +92,7 @@ def load_library(path=LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
     lib.tg_gemm_config.restype = i32
-    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32, ip, ip, ip, ip, ip, ip, ip, ip, ip]
+    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32] + [ip] * 11
     lib.tg_gemm_launch_shape.restype = i32
     lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
                                              i64]
@@ -213,13 +213,16 @@ def tg_gemm_config():
     return dict(zip(keys, (v.value for v in vals)))
 
 
-def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False, dynamic=False):
-    """The persistent launch the library uses for M x N x K on the current device."""
-    vals = [ctypes.c_int() for _ in range(9)]
-    _check(load_library().tg_gemm_launch_shape(M, N, K, _variant(variant, plain, False, dynamic),
-                                               *[ctypes.byref(v) for v in vals]))
+def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False, dynamic=False,
+                         column_major=False, group=None):
+    """The persistent launch (and traversal) the library uses for M x N x K on the current
+    device."""
+    vals = [ctypes.c_int() for _ in range(11)]
+    _check(load_library().tg_gemm_launch_shape(
+        M, N, K, _variant(variant, plain, column_major, dynamic, group),
+        *[ctypes.byref(v) for v in vals]))
     keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas",
-            "split_from", "units")
+            "split_from", "units", "group", "column_major")
     return dict(zip(keys, (v.value for v in vals)))
 
 

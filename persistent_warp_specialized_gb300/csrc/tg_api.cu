@@ -189,18 +189,45 @@ int auto_variant(int64_t M, int64_t N, int64_t /*K*/, int max_pairs) {
   return (max_pairs > 0 && pair_tiles >= max_pairs) ? TG_VARIANT_PAIR : TG_VARIANT_SINGLE;
 }
 
-// The dense GEMM's choice: the wide pair kernel (256 x 512 tiles) once its tiles fill at least
-// four waves of resident pairs -- measured faster there (8192^3 +1.8 % in bursts, +2.9 % over
-// 1000 back-to-back launches; K = 16384 +3.9 %), while with fewer waves its coarser last wave
-// costs more than it gains (4096^3 -8 %) -- else as auto_variant.
+// The dense GEMM's choice: the wide pair kernel (256 x 512 tiles) when its tiles fill at least
+// one wave of resident pairs and K is long enough for the once-per-tile drain of its single
+// accumulator to stay small, else as auto_variant.  Measured on GB300 (same box, medians of 5
+// alternating bursts, pair / wide TFLOP/s): K >= 6144 favours wide at every size tried (6144^3
+// 1835 / 1894, 4096 x 4096 x 8192 1711 / 1763 at 1.7 waves, 4096 x 8192 x 8192 1838 / 1874,
+// 8192^3 +2.6 %); K = 4096 ties (8192 x 8192 1904 / 1894, 12288 x 12288 1937 / 1939, 6144 x 6144
+// 1858 / 1862), so wide is kept there only for four waves or more; K = 2048 favours the pair
+// kernel (8192 x 8192 1858 / 1773).
 int auto_variant_dense(int64_t M, int64_t N, int64_t K, int max_pairs) {
   const int64_t wide_tiles =
       ((M + tg::kPairBM - 1) / tg::kPairBM) * ((N + tg::kWideBN - 1) / tg::kWideBN);
-  if (max_pairs > 0 && wide_tiles >= 4 * int64_t(max_pairs)) return TG_VARIANT_PAIR_WIDE;
+  if (max_pairs > 0 && ((K >= 6144 && wide_tiles >= max_pairs) ||
+                        (K >= 4096 && wide_tiles >= 4 * int64_t(max_pairs))))
+    return TG_VARIANT_PAIR_WIDE;
   return auto_variant(M, N, K, max_pairs);
 }
 
 bool pair_variant(int v) { return v == TG_VARIANT_PAIR || v == TG_VARIANT_PAIR_WIDE; }
+
+// The traversal TG_VARIANT_AUTO gives the dense kernel it picks when the caller names neither
+// an order nor a group width (the page's scheduler options ``column_major`` and
+// ``swizzle_size``).  When all of B fits in half of the L2, whole rows of tiles (group = the
+// number of N-tiles) read each row slab of A from DRAM once while B stays resident; when only A
+// fits, whole columns do the same with the roles exchanged; otherwise the page's grouped order
+// of width 8.  Measured on GB300 (CTA-pair kernel, medians of 3 rounds): 4096^3 rows 1797 vs
+// groups of 8 1745 TFLOP/s, 4000 x 7000 x 2048 rows of 16 1637 vs 1612; at 8192^3 (B 128 MiB)
+// groups of 8 stay best.
+struct Raster {
+  uint32_t group, column_major;
+};
+constexpr uint64_t kHalfL2Bytes = 64ull << 20;
+
+Raster auto_raster(int64_t M, int64_t N, int64_t K, uint32_t m_tiles, uint32_t n_tiles) {
+  const uint64_t a_bytes = uint64_t(M) * K * tg::kElemBytes;
+  const uint64_t b_bytes = uint64_t(K) * N * tg::kElemBytes;
+  if (b_bytes <= kHalfL2Bytes) return {n_tiles < 255u ? n_tiles : 255u, 0u};
+  if (a_bytes <= kHalfL2Bytes) return {m_tiles < 255u ? m_tiles : 255u, 1u};
+  return {static_cast<uint32_t>(tg::kGroup), 0u};
+}
 
 struct Shape {
   uint32_t tile_m, tile_n, m_tiles, n_tiles, workers, ctas, split_from, units;
@@ -246,15 +273,23 @@ uint32_t group_of(int v) {
   return g ? g : static_cast<uint32_t>(tg::kGroup);
 }
 
+// True when TG_VARIANT_AUTO also chooses the traversal: the caller named no order, no group
+// width and not the page's plain traversal.
+bool auto_traversal(int variant) {
+  return (variant & ~kScheduleFlags) == TG_VARIANT_AUTO &&
+         (variant & (TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | kGroupBits)) == 0;
+}
+
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
               void* stream, int variant, bool debug, int32_t* trace, uint64_t watchdog_ns,
               int64_t inject) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
-  const uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
+  uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
-  const uint32_t group = group_of(variant);
+  uint32_t group = group_of(variant);
   const uint32_t epi_direct = (variant & TG_EPILOGUE_DIRECT) ? 1u : 0u;
+  const bool choose_traversal = auto_traversal(variant);
   variant &= ~kScheduleFlags;
   bool nothing = false;
   int rc = validate(A, B, C, M, N, K, dtype, &nothing);
@@ -283,6 +318,11 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
   const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
+  if (choose_traversal) {
+    const Raster r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles);
+    group = r.group;
+    column_major = r.column_major;
+  }
   l.m_blocks = sh.m_tiles;
   l.n_blocks = sh.n_tiles;
   l.split_from = sh.split_from;
@@ -529,10 +569,13 @@ int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev, int
 
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
-                         int* ctas, int* split_from, int* units) {
+                         int* ctas, int* split_from, int* units, int* group,
+                         int* column_major) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
+  const bool choose_traversal = auto_traversal(variant);
+  Raster r = {group_of(variant), (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u};
   variant &= ~kScheduleFlags;
   if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
@@ -543,7 +586,10 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
   if (dynamic && variant != TG_VARIANT_SINGLE)
     return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
   const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
+  if (choose_traversal) r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles);
   if (variant_out) *variant_out = variant;
+  if (group) *group = static_cast<int>(r.group);
+  if (column_major) *column_major = static_cast<int>(r.column_major);
   if (tile_m) *tile_m = static_cast<int>(sh.tile_m);
   if (tile_n) *tile_n = static_cast<int>(sh.tile_n);
   if (m_tiles) *m_tiles = static_cast<int>(sh.m_tiles);

@@ -60,6 +60,13 @@ struct GemmParams {
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
 };
 
+// Debug fault injection: ``inject`` = cta * 2^32 + phase names a pipeline phase that the producer
+// of CTA ``cta`` skips (-1: none).
+__device__ __forceinline__ bool injected_skip(int64_t inject, uint64_t phase) {
+  return inject >= 0 && (static_cast<uint64_t>(inject) & 0xFFFFFFFFull) == phase &&
+         (static_cast<uint64_t>(inject) >> 32) == blockIdx.x;
+}
+
 // Per-device status word of the watchdog (bits: kRole*).  Read and cleared by the host.
 __device__ unsigned int g_watchdog_status = 0;
 
@@ -125,20 +132,27 @@ __device__ __forceinline__ uint32_t pack_out(uint32_t lo_bits, uint32_t hi_bits)
   }
 }
 
-// Stores this warp's 32 rows x 64 columns of the accumulator (v: lane = row, 64 columns),
-// converted to the output type, at rows row0 .. row0 + 31 and columns x .. x + 63 of C.
-// Rows >= M and columns >= N are not written.
+// Converts one 64-column chunk of a warp's accumulator rows (v: lane = row, fp32 bits) to the
+// output type: pk[i] holds columns 2i and 2i + 1 (round to nearest even).
+template <int DT>
+__device__ __forceinline__ void pack_chunk(const uint32_t (&v)[64], uint32_t (&pk)[32]) {
+#pragma unroll
+  for (uint32_t i = 0; i < 32; ++i) pk[i] = pack_out<DT>(v[2 * i], v[2 * i + 1]);
+}
+
+// Stores this warp's 32 rows x 64 columns, already converted (pk: lane = row, 32 words of two
+// output values), at rows row0 .. row0 + 31 and columns x .. x + 63 of C.  Rows >= M and
+// columns >= N are not written.
 //  * staged (default): each lane writes its row as eight 16-byte chunks into a 128-byte
 //    swizzled staging buffer (chunk c of row r at chunk c ^ (r % 8): conflict-free), the
 //    warp fences the writes into the async proxy, and lane 0 issues one TMA store, which
 //    clips at the tensor's edge.  Two buffers per warp alternate; before one is rewritten,
 //    lane 0 waits until the store that read it is done.  One bulk group per chunk.
 //  * direct (p.epi_direct): each lane stores its row's 128 bytes with 16-byte stores.
-template <int DT>
-__device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], uint32_t lane,
-                                                     uint32_t sbuf, const CUtensorMap* tmC,
-                                                     const GemmParams& p, int32_t row0,
-                                                     int32_t x) {
+__device__ __forceinline__ void epilogue_store_packed(const uint32_t (&pk)[32], uint32_t lane,
+                                                      uint32_t sbuf, const CUtensorMap* tmC,
+                                                      const GemmParams& p, int32_t row0,
+                                                      int32_t x) {
   if (p.epi_direct) {
     const int32_t row = row0 + static_cast<int32_t>(lane);
     if (row < static_cast<int32_t>(p.M)) {
@@ -147,10 +161,7 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], ui
 #pragma unroll
       for (uint32_t c = 0; c < 8; ++c) {
         if (x + static_cast<int32_t>(8 * c) < static_cast<int32_t>(p.N))
-          st_global_v4(base + 16 * c, pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
-                       pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
-                       pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
-                       pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
+          st_global_v4(base + 16 * c, pk[4 * c + 0], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
     }
   } else {
@@ -158,12 +169,9 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], ui
     __syncwarp();
     const uint32_t row_addr = sbuf + lane * 128u;
 #pragma unroll
-    for (uint32_t c = 0; c < 8; ++c) {
-      st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4), pack_out<DT>(v[8 * c + 0], v[8 * c + 1]),
-                   pack_out<DT>(v[8 * c + 2], v[8 * c + 3]),
-                   pack_out<DT>(v[8 * c + 4], v[8 * c + 5]),
-                   pack_out<DT>(v[8 * c + 6], v[8 * c + 7]));
-    }
+    for (uint32_t c = 0; c < 8; ++c)
+      st_shared_v4(row_addr + ((c ^ (lane & 7u)) << 4), pk[4 * c + 0], pk[4 * c + 1],
+                   pk[4 * c + 2], pk[4 * c + 3]);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
@@ -173,6 +181,18 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], ui
     }
   }
   __syncwarp();   // converged for the next warp-collective tcgen05.ld
+}
+
+// Converts and stores one 64-column chunk of the accumulator (v: lane = row, fp32 bits); see
+// epilogue_store_packed.
+template <int DT>
+__device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v)[64], uint32_t lane,
+                                                     uint32_t sbuf, const CUtensorMap* tmC,
+                                                     const GemmParams& p, int32_t row0,
+                                                     int32_t x) {
+  uint32_t pk[32];
+  pack_chunk<DT>(v, pk);
+  epilogue_store_packed(pk, lane, sbuf, tmC, p, row0, x);
 }
 
 // Dynamic persistence (cluster launch control).  The grid holds one CTA per work unit; a CTA
@@ -315,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           pending &= ~(1u << s);
-          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
-            continue;  // injected fault: this phase is never filled
+          if (DEBUG && injected_skip(p.inject_skip_phase, phase))
+            continue;  // injected fault: this CTA never fills this phase
           const uint32_t full = bar_loaded + 8u * s;
           mbar_arrive_expect_tx(full, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kBK;

@@ -32,12 +32,24 @@
 
 namespace tg {
 
+// What a producer of a CTA pair last put on each ring slot, for the abort path: the phase
+// (low 32 bits), 2 | the phase's parity on the slot (0: the slot was never filled), and this
+// CTA's bytes of that fill.  Each CTA keeps its own in its shared memory.
+template <int S>
+struct PairFills {
+  uint32_t phase[S];
+  uint32_t par[S];
+  uint32_t bytes[S];
+};
+
 struct __align__(8) PairCtl {
   uint64_t loaded[kPairStages];      // used in the even CTA only
   uint64_t consumed[kPairStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];            // used in the even CTA only (count 256)
   uint64_t drain;
+  uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
+  PairFills<kPairStages> fills;
   uint32_t tmem_base;
   int abort;
 };
@@ -67,9 +79,52 @@ __device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
+template <int S>
+__device__ __forceinline__ void record_fill(PairFills<S>& f, uint32_t s, uint64_t phase,
+                                            uint32_t par, uint32_t bytes) {
+  f.phase[s] = static_cast<uint32_t>(phase);
+  f.par[s] = 2u | par;
+  f.bytes[s] = bytes;
+}
+
+// The abort path of a CTA pair: run by one thread of the even CTA once every role of that CTA
+// has left its loop, before the closing cluster barrier (which the odd CTA cannot pass any
+// earlier).  Every TMA load of either CTA completes on the even CTA's ``loaded`` barriers; this
+// waits until all of them have landed, so neither CTA leaves while a copy may still write its
+// shared memory.  Once the odd producer has said on ``bar_odd_done`` that it has stopped, its
+// fill records are read over DSMEM and compared slot by slot with this CTA's:
+//  * the odd CTA filled a phase this CTA never armed (this producer stopped one ring earlier):
+//    arm that phase with the odd CTA's bytes and wait for it;
+//  * this CTA armed a phase the odd CTA never filled: count the odd CTA's share as done (both
+//    CTAs load the same shapes, so it equals this CTA's bytes) and wait for this CTA's loads;
+//  * both filled the same phase: wait for it.
+// The two producers' last fills of a slot are the same phase or one ring apart, since each
+// waits for the slot to be consumed, and consuming needs both CTAs' bytes.
+template <int S>
+__device__ void pair_drain_fills(uint32_t bar_loaded, const PairFills<S>& own,
+                                 uint32_t odd_fills, uint32_t bar_odd_done, uint64_t limit) {
   const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) {
+  while (!mbar_try_wait_cluster(bar_odd_done, 0)) {
+    if (globaltimer_ns() - t0 > limit) {
+      atomicOr(&g_watchdog_status, kRoleDrain);
+      return;
+    }
+  }
+#pragma unroll 1
+  for (uint32_t s = 0; s < static_cast<uint32_t>(S); ++s) {
+    const uint32_t e_par = own.par[s];
+    const uint32_t o_par = ld_shared_cluster_u32(odd_fills + 4u * (S + s));
+    if (!(e_par & 2u) && !(o_par & 2u)) continue;
+    const uint32_t bar = bar_loaded + 8u * s;
+    const uint32_t o_phase = ld_shared_cluster_u32(odd_fills + 4u * s);
+    const int32_t ahead = static_cast<int32_t>(o_phase - own.phase[s]);
+    if ((o_par & 2u) && (!(e_par & 2u) || ahead > 0)) {
+      mbar_arrive_expect_tx(bar, ld_shared_cluster_u32(odd_fills + 4u * (2 * S + s)));
+      wait_bounded(bar, o_par & 1u, limit, kRoleDrain);
+    } else {
+      if (!(o_par & 2u) || ahead != 0) mbar_complete_tx(bar, own.bytes[s]);
+      wait_bounded(bar, e_par & 1u, limit, kRoleDrain);
+    }
   }
 }
 
@@ -110,6 +165,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_tmem_empty + 8u * b, 2 * kEpiThreads);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(smem_u32(&ctl.odd_done), 1);
+#pragma unroll
+    for (int st = 0; st < kPairStages; ++st) ctl.fills.par[st] = 0;
     ctl.abort = 0;
     fence_mbarrier_init();
   }
@@ -146,7 +204,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       sched.init(pair);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
-      uint32_t pending = 0, pending_par = 0;
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
@@ -168,9 +225,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          pending &= ~(1u << s);
-          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
-            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          if (DEBUG && injected_skip(p.inject_skip_phase, phase))
+            continue;  // injected fault: this CTA never arms or fills this phase
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kPairBK;
@@ -193,22 +249,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             else
               tma_load_2d_pair(dst, &tmB, full_even, nx, kx);
           }
-          pending |= 1u << s;
-          pending_par = (pending_par & ~(1u << s)) | (par << s);
+          record_fill(ctl.fills, s, phase, par, tx_bytes / 2u);
         }
         sched.next_tile();
       }
-      if (!ok) {
-        if (rank == 0) {
-          for (uint32_t s = 0; s < kPairStages; ++s)
-            if ((pending >> s) & 1u)
-              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
-        } else if (pending) {
-          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
-          // give them time to land before this CTA may leave
-          spin_ns(limit < 1000000ull ? limit : 1000000ull);
-        }
-      }
+      // the odd producer has stopped filling: its records are final (see pair_drain_fills)
+      if (rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.odd_done), 0));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -307,6 +353,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  __syncthreads();   // every role of this CTA has left its loop
+  if (rank == 0 && warp == 0 && lane == 0 && *abort_flag)
+    pair_drain_fills(bar_loaded, ctl.fills, mapa_shared(smem_u32(&ctl.fills), 1),
+                     smem_u32(&ctl.odd_done), limit);
   tcgen05_fence_before_sync();
   cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
   if (warp == 2) {

@@ -11,10 +11,14 @@
 //   * a stage holds as much MMA work as the 256 x 256 kernel's 128-deep stage (0.68 us at the
 //     bf16 peak), and a refill has three stages instead of two to arrive;
 //   * the tail split's half units are 256 x 256 (whole N-halves) rather than 256 x 128;
-//   * there is one accumulator (all 512 TMEM columns): the epilogue hands each N-half back on
-//     its own barrier (tmem_empty[h]) once it has read it, and the MMA waits for half h only
-//     before its first write of the next unit.  A half unit hands back its unused half at once,
-//     so both barriers complete once per unit and the parity of unit w is (w & 1) ^ 1.
+//   * there is one accumulator (all 512 TMEM columns), so the next unit's MMAs wait for the
+//     epilogue to read the previous one out.  To keep that wait short, the epilogue copies a
+//     whole N-half into registers (converted to the output type: 128 words per thread) and
+//     hands it back on its own barrier (tmem_empty[h]) before storing any of it; the MMA waits
+//     for half 0 before its first k-block and for half 1 only after N-half 0 of the first
+//     kWideDefer k-blocks, whose ring slots it releases once half 1 has caught up on them.  A
+//     half unit hands back its unused half at once, so both barriers complete once per unit
+//     and the parity of unit w is (w & 1) ^ 1.
 // Everything else -- the scheduler, the single iteration clock with slot phase % S, the odd
 // CTA's loads completing on the even CTA's barrier, multicast commits, bounded waits with the
 // pair abort, the TMA-store epilogue -- is the pair kernel's.  Included by exactly one
@@ -32,6 +36,8 @@ struct __align__(8) WideCtl {
   uint64_t tmem_full;
   uint64_t tmem_empty[2];            // per N-half; used in the even CTA only (count 256)
   uint64_t drain;
+  uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
+  PairFills<kWideStages> fills;
   uint32_t tmem_base;
   int abort;
 };
@@ -71,6 +77,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_tmem_empty, 2 * kEpiThreads);
     mbar_init(bar_tmem_empty + 8u, 2 * kEpiThreads);
     mbar_init(bar_drain, 1);
+    mbar_init(smem_u32(&ctl.odd_done), 1);
+#pragma unroll
+    for (int st = 0; st < kWideStages; ++st) ctl.fills.par[st] = 0;
     ctl.abort = 0;
     fence_mbarrier_init();
   }
@@ -105,7 +114,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
                                     p.total_units, p.column_major);
       sched.init(pair);
-      uint32_t pending = 0, pending_par = 0;
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
@@ -123,9 +131,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          pending &= ~(1u << s);
-          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
-            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          if (DEBUG && injected_skip(p.inject_skip_phase, phase))
+            continue;  // injected fault: this CTA never arms or fills this phase
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, tx_bytes);
           const int32_t kx = static_cast<int32_t>(k) * kWideBK;
@@ -141,22 +148,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d_pair(dst, &tmB, full_even, nx, kx);
             }
           }
-          pending |= 1u << s;
-          pending_par = (pending_par & ~(1u << s)) | (par << s);
+          record_fill(ctl.fills, s, phase, par, tx_bytes / 2u);
         }
         sched.next_tile();
       }
-      if (!ok) {
-        if (rank == 0) {
-          for (uint32_t s = 0; s < kWideStages; ++s)
-            if ((pending >> s) & 1u)
-              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
-        } else if (pending) {
-          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
-          // give them time to land before this CTA may leave
-          spin_ns(limit < 1000000ull ? limit : 1000000ull);
-        }
-      }
+      // the odd producer has stopped filling: its records are final (see pair_drain_fills)
+      if (rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.odd_done), 0));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -167,11 +164,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     p.total_units, p.column_major);
       sched.init(pair);
       bool ok = true;
+      // MMAs of N-half h for the k-block in ring slot s (k: its index within the unit)
+      auto issue_half = [&](uint32_t s, uint32_t h, uint32_t k) {
+        const uint32_t a_addr = sA0 + s * kWideStageBytes;
+        const uint32_t b_addr = sB0 + s * kWideStageBytes + 2u * h * kWideBChunkBytes;
+#pragma unroll
+        for (uint32_t kk = 0; kk < kWideBK / kUmmaK; ++kk) {
+          const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
+          const uint64_t b_desc =
+              smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kWideBChunkBytes, 1024);
+          umma_f16_pair(tmem_base + h * kBN, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+        }
+      };
       while (ok && sched.valid()) {
         const uint32_t w = sched.current_iter;
         const uint32_t halves = sched.part >= 0 ? 1u : 2u;
+        // N-half 1 of the first ``defer`` k-blocks waits until the epilogue has handed half 1
+        // back; those slots are released only once both halves have read them
+        const uint32_t defer =
+            halves == 2u ? (kWideDefer < p.k_blocks ? kWideDefer : p.k_blocks - 1u) : 0u;
+        const uint64_t phase0 = static_cast<uint64_t>(w) * k_blocks;
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
-          const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
+          const uint64_t phase = phase0 + k;
           const uint32_t s = static_cast<uint32_t>(phase % kWideStages);
           const uint32_t par = static_cast<uint32_t>((phase / kWideStages) & 1u);
           if (!pair_wait_or_abort(bar_loaded + 8u * s, par, abort_flag, peer_abort, limit,
@@ -180,29 +194,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tcgen05_fence_after_sync();
-          const uint32_t a_addr = sA0 + s * kWideStageBytes;
-          const uint32_t b_addr = sB0 + s * kWideStageBytes;
-#pragma unroll
-          for (uint32_t h = 0; h < 2; ++h) {
-            if (h >= halves) break;
-            if (k == 0) {
-              // half h of the previous unit's accumulator has been read out by both epilogues
-              if (!pair_wait_or_abort(bar_tmem_empty + 8u * h, (w & 1u) ^ 1u, abort_flag,
-                                      peer_abort, limit, kRoleMma)) {
-                ok = false;
-                break;
-              }
-              tcgen05_fence_after_sync();
+          if (k == 0) {
+            // half 0 of the previous unit's accumulator has been read out by both epilogues
+            if (!pair_wait_or_abort(bar_tmem_empty, (w & 1u) ^ 1u, abort_flag, peer_abort,
+                                    limit, kRoleMma)) {
+              ok = false;
+              break;
             }
-#pragma unroll
-            for (uint32_t kk = 0; kk < kWideBK / kUmmaK; ++kk) {
-              const uint64_t a_desc = smem_desc_sw128(a_addr + kk * kUmmaK * kElemBytes, 16, 1024);
-              const uint64_t b_desc = smem_desc_sw128(
-                  b_addr + 2u * h * kWideBChunkBytes + kk * kUmmaK * 128u, kWideBChunkBytes, 1024);
-              umma_f16_pair(tmem_base + h * kBN, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+            tcgen05_fence_after_sync();
+          }
+          issue_half(s, 0, k);
+          if (halves == 1u) {
+            umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
+            continue;
+          }
+          if (k < defer) continue;   // slot s stays held until half 1 has read it
+          if (k == defer) {
+            if (!pair_wait_or_abort(bar_tmem_empty + 8u, (w & 1u) ^ 1u, abort_flag, peer_abort,
+                                    limit, kRoleMma)) {
+              ok = false;
+              break;
+            }
+            tcgen05_fence_after_sync();
+            for (uint32_t j = 0; j < defer; ++j) {   // catch half 1 up, releasing each slot
+              const uint32_t sj = static_cast<uint32_t>((phase0 + j) % kWideStages);
+              issue_half(sj, 1, j);
+              umma_commit_pair_multicast(bar_consumed + 8u * sj, 0x3);
             }
           }
-          if (!ok) break;
+          issue_half(s, 1, k);
           umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
         }
         if (!ok) break;
@@ -238,18 +258,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));   // unused half
           continue;
         }
-#pragma unroll 1
-        for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
+        // the whole N-half into registers, converted (4 chunks x 32 words per lane), then
+        // hand it back to the MMA before any of it is stored
+        uint32_t pk[kBN / kEpiN][kEpiN / 2];
+#pragma unroll
+        for (uint32_t j = 0; j < kBN / kEpiN; ++j) {
           uint32_t v[64];
           tmem_ld_32x32b_x64(t_row + h * kBN + j * kEpiN, v);
-          if (j == kBN / kEpiN - 1) {
-            // half h fully in registers: hand it back to the MMA before storing
-            tcgen05_fence_before_sync();
-            mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));
-          }
+          pack_chunk<DT>(v, pk[j]);
+        }
+        tcgen05_fence_before_sync();
+        mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));
+#pragma unroll
+        for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
           const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
-          epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
-                                   col0 + static_cast<int32_t>(h * kBN + j * kEpiN));
+          epilogue_store_packed(pk[j], lane, sbuf, &tmC, p, row0,
+                                col0 + static_cast<int32_t>(h * kBN + j * kEpiN));
         }
       }
       if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
@@ -266,6 +290,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  __syncthreads();   // every role of this CTA has left its loop
+  if (rank == 0 && warp == 0 && lane == 0 && *abort_flag)
+    pair_drain_fills(bar_loaded, ctl.fills, mapa_shared(smem_u32(&ctl.fills), 1),
+                     smem_u32(&ctl.odd_done), limit);
   tcgen05_fence_before_sync();
   cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
   if (warp == 2) {

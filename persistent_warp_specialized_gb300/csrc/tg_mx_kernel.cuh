@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           pending &= ~(1u << s);
-          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
+          if (DEBUG && injected_skip(p.inject_skip_phase, phase))
             continue;  // injected fault: the operands of this phase are never loaded
           const uint32_t full = bar_loaded + 8u * s;
           const int32_t kx = static_cast<int32_t>(k * kMxBK);

@@ -39,6 +39,8 @@ struct __align__(8) MxPairCtl {
   uint64_t tmem_full;
   uint64_t tmem_empty;               // used in the even CTA only (count 256)
   uint64_t drain;
+  uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
+  PairFills<kMxPairStages> fills;
   uint32_t tmem_base;
   int abort;
 };
@@ -82,6 +84,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_tmem_full, 1);
     mbar_init(bar_tmem_empty, 2 * kEpiThreads);
     mbar_init(bar_drain, 1);
+    mbar_init(smem_u32(&ctl.odd_done), 1);
+#pragma unroll
+    for (int st = 0; st < kMxPairStages; ++st) ctl.fills.par[st] = 0;
     ctl.abort = 0;
     fence_mbarrier_init();
   }
@@ -118,7 +123,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
                                     p.total_units, p.column_major);
       sched.init(pair);
-      uint32_t pending = 0, pending_par = 0;
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
@@ -137,9 +141,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          pending &= ~(1u << s);
-          if (DEBUG && static_cast<int64_t>(phase) == p.inject_skip_phase && blockIdx.x == 0)
-            continue;  // injected fault: the even CTA of pair 0 never arms or fills this phase
+          if (DEBUG && injected_skip(p.inject_skip_phase, phase))
+            continue;  // injected fault: this CTA never arms or fills this phase
           const uint32_t full_even = mapa_shared(bar_loaded + 8u * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(bar_loaded + 8u * s, kMxPairTxBytes);
 #pragma unroll
@@ -155,22 +158,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(atom + kMxSfAtomBytes, &tmSFB, full_even, 0,
                              static_cast<int32_t>(k * p.sfb_blocks) + sfb_row);
           }
-          pending |= 1u << s;
-          pending_par = (pending_par & ~(1u << s)) | (par << s);
+          record_fill(ctl.fills, s, phase, par, kMxPairTxBytes / 2u);
         }
         sched.next_tile();
       }
-      if (!ok) {
-        if (rank == 0) {
-          for (uint32_t s = 0; s < kMxPairStages; ++s)
-            if ((pending >> s) & 1u)
-              wait_bounded(bar_loaded + 8u * s, (pending_par >> s) & 1u, limit, kRoleDrain);
-        } else if (pending) {
-          // the odd CTA's loads complete on the even CTA's barrier, which it cannot wait on:
-          // give them time to land before this CTA may leave
-          spin_ns(limit < 1000000ull ? limit : 1000000ull);
-        }
-      }
+      // the odd producer has stopped filling: its records are final (see pair_drain_fills)
+      if (rank == 1) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl.odd_done), 0));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -281,6 +274,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  __syncthreads();   // every role of this CTA has left its loop
+  if (rank == 0 && warp == 0 && lane == 0 && *abort_flag)
+    pair_drain_fills(bar_loaded, ctl.fills, mapa_shared(smem_u32(&ctl.fills), 1),
+                     smem_u32(&ctl.odd_done), limit);
   tcgen05_fence_before_sync();
   cluster_sync();   // neither CTA leaves while the pair may still touch its smem or TMEM
   if (warp == 2) {

@@ -18,6 +18,15 @@ constexpr uint32_t kWideABytes = kBM * kWideBK * kElemBytes;                 // 
 constexpr uint32_t kWideBChunkBytes = kWideBK * kBChunkCols * kElemBytes;    // 8 KiB
 constexpr uint32_t kWideStageBytes = kWideABytes + 4 * kWideBChunkBytes;    // 48 KiB per CTA
 constexpr uint32_t kWideSmemBytes = kSmemAlignSlack + kWideStages * kWideStageBytes + kEpiSmemBytes;
+// At the start of a unit the MMA may run N-half 0 of the first kWideDefer k-blocks before the
+// epilogue has handed N-half 1 of the previous unit back (those ring slots are released once
+// half 1 has read them too).  One k-block measured best on GB300 (8192^3: 2004-2007 TFLOP/s
+// against 1995-1997 with none; two or three gained nothing more, since held slots delay refills).
+#ifndef TG_WIDE_DEFER
+#define TG_WIDE_DEFER 1
+#endif
+constexpr uint32_t kWideDefer = TG_WIDE_DEFER;
+static_assert(kWideDefer < kWideStages, "deferred k-blocks hold ring slots");
 static_assert(kWideSmemBytes + 256 <= 232448, "shared memory per CTA (wide pair variant)");
 static_assert(kWideBK == kKAtom, "a wide stage holds one 128-byte swizzle atom of A");
 static_assert(2 * kBN <= (int)kTmemCols, "the wide accumulator spans both TMEM halves");

@@ -157,8 +157,10 @@ def test_kernel_followed_the_schedule(M, N, K, plain, column_major, variant):
     assert np.array_equal(got_c, ref_bits(a, sa, b, sb))
 
 
-@pytest.mark.parametrize("variant", MX_VARIANTS)
-def test_watchdog_fires_and_context_survives(variant):
+@pytest.mark.parametrize("variant,cta", [(v, 0) for v in MX_VARIANTS] + [("pair", 1)])
+def test_watchdog_fires_and_context_survives(variant, cta):
+    # CTA ``cta``'s producer skips phase 2; in the pair, CTA 1 (odd) leaves a phase that only
+    # the even CTA armed, which the abort path must still see land
     M, N, K = 512, 512, 1024
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=1)
     dev = device_inputs(a, sa, b, sb)
@@ -166,7 +168,7 @@ def test_watchdog_fires_and_context_survives(variant):
     with pytest.raises(tg.TgError) as e:
         # phase 2 exists in both kernels (single: k-blocks 0..7; pair: stages of 2 k-blocks)
         tg.tg_gemm_mxfp8_debug(*dev, c, M, N, K, "bf16", variant=variant, watchdog_ns=20_000_000,
-                               inject_skip_phase=2)
+                               inject_skip_phase=(cta << 32) + 2)
     assert e.value.code == tg.TG_ERR_TIMEOUT
     assert tg.tg_device_status() == 0
     assert np.array_equal(run_mx(a, sa, b, sb, variant=variant), ref_bits(a, sa, b, sb))

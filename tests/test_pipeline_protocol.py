@@ -452,3 +452,153 @@ def test_wide_half_unit_must_hand_back_its_unused_half():
     # without the immediate hand-back, the unit after a half unit waits forever on half 1
     results = [run_wide_accumulator([2, 1, 2], 2, seed, release_unused=False) for seed in range(20)]
     assert all(r is not None and r.startswith("deadlock") for r in results)
+
+
+# ---------------------------------------------------------------- wide pair: ring + accumulator
+# The wide pair kernel's MMA role ties the operand ring to the accumulator hand-back: at the
+# start of a whole unit it may run N-half 0 of the first ``defer`` k-blocks before the epilogues
+# have handed N-half 1 of the previous unit back, holding those ring slots until half 1 has
+# read them too (kWideDefer in tg_wide_config.h).  This model runs the producer, the MMA role
+# in the kernel's issue order and both CTAs' epilogues as coroutines on modelled mbarriers,
+# interleaved at random, and checks that every MMA reads the k-block of its own phase, that a
+# slot is refilled only after every half that needs it has read it, that each half of the
+# accumulator receives its unit's k-blocks in order before being read and is read only once
+# complete, and that nothing deadlocks.
+
+
+def run_wide_pipeline(halves, k_blocks, S, defer, seed, catch_up_commits=True):
+    rng = random.Random(seed)
+    units = len(halves)
+    loaded = [Barrier() for _ in range(S)]
+    consumed = [Barrier() for _ in range(S)]
+    full = [Barrier(), Barrier()]
+    empty = [CountBarrier(2), CountBarrier(2)]
+    data = [None] * S
+    need = [set() for _ in range(S)]        # halves that still have to read the slot
+    acc = [[None, None], [None, None]]      # [unit, k-blocks written, read?] per CTA and half
+    errors = []
+
+    def fail(msg):
+        errors.append(msg)
+        raise StopIteration
+
+    def producer():
+        for w in range(units):
+            for k in range(k_blocks):
+                ph = w * k_blocks + k
+                s = slot_of(ph, S)
+                yield consumed[s], parity_of(ph, S) ^ 1
+                if need[s]:
+                    errors.append(f"slot {s} refilled (phase {ph}) before halves {need[s]} read it")
+                    return
+                data[s] = ph
+                need[s] = set(range(halves[w]))
+                loaded[s].complete()
+
+    def op(w, h, k):
+        ph = w * k_blocks + k
+        s = slot_of(ph, S)
+        if data[s] != ph:
+            return f"unit {w} half {h} k {k} read slot {s} holding phase {data[s]}"
+        need[s].discard(h)
+        for c in (0, 1):
+            cur = acc[c][h]
+            if k == 0:
+                if cur is not None and not cur[2]:
+                    return f"unit {w} overwrote half {h} of CTA {c} before unit {cur[0]} was read"
+                acc[c][h] = [w, 1, False]
+            else:
+                if cur is None or cur[0] != w or cur[1] != k:
+                    return f"unit {w} half {h} k-block {k} accumulated onto {cur}"
+                cur[1] += 1
+        return None
+
+    def commit(w, k):
+        s = slot_of(w * k_blocks + k, S)
+        if need[s]:
+            return f"slot {s} released with halves {need[s]} unread"
+        consumed[s].complete()
+        return None
+
+    def mma():
+        for w in range(units):
+            d = min(defer, k_blocks - 1) if halves[w] == 2 else 0
+            for k in range(k_blocks):
+                ph = w * k_blocks + k
+                yield loaded[slot_of(ph, S)], parity_of(ph, S)
+                if k == 0:
+                    yield empty[0], (w & 1) ^ 1
+                for m in (op(w, 0, k),):
+                    if m:
+                        errors.append(m)
+                        return
+                if halves[w] == 1:
+                    m = commit(w, k)
+                    if m:
+                        errors.append(m)
+                        return
+                    continue
+                if k < d:
+                    continue
+                if k == d:
+                    yield empty[1], (w & 1) ^ 1
+                    for j in range(d):
+                        m = op(w, 1, j) or (commit(w, j) if catch_up_commits else None)
+                        if m:
+                            errors.append(m)
+                            return
+                m = op(w, 1, k) or commit(w, k)
+                if m:
+                    errors.append(m)
+                    return
+            full[0].complete()
+            full[1].complete()
+
+    def epilogue(c):
+        for w in range(units):
+            yield full[c], w & 1
+            for h in (0, 1):
+                if h < halves[w]:
+                    cur = acc[c][h]
+                    if cur is None or cur[0] != w or cur[1] != k_blocks:
+                        errors.append(f"CTA {c} read half {h} of unit {w} as {cur}")
+                        return
+                    cur[2] = True
+                empty[h].arrive()
+
+    roles = {"producer": producer(), "mma": mma(), "epi0": epilogue(0), "epi1": epilogue(1)}
+    waits = {}
+    for name, g in list(roles.items()):
+        waits[name] = next(g, None)
+    while True:
+        if errors:
+            return errors[0]
+        live = {n: wt for n, wt in waits.items() if wt is not None}
+        if not live:
+            return None
+        ready = [n for n, (bar, par) in live.items() if bar.passes(par)]
+        if not ready:
+            return f"deadlock: waiting {sorted(live)}"
+        n = rng.choice(ready)
+        waits[n] = next(roles[n], None)
+
+
+@pytest.mark.parametrize("defer", [0, 1, 2, 3])
+@pytest.mark.parametrize("halves", [[2, 2, 2], [2, 1, 2], [1, 2, 2, 1], [2], [1, 1]])
+@pytest.mark.parametrize("k_blocks", [1, 2, 3, 4, 7])
+def test_wide_ring_and_accumulator_hold_with_deferred_half(defer, halves, k_blocks):
+    for seed in range(25):
+        assert run_wide_pipeline(halves, k_blocks, 4, defer, seed) is None
+
+
+def test_wide_deferral_of_every_slot_deadlocks():
+    # holding all S slots for half 1 leaves the producer nothing to refill: the reason the
+    # deferral is kept below the ring depth
+    results = [run_wide_pipeline([2, 2, 2], 8, 4, 4, seed) for seed in range(10)]
+    assert all(r is not None and r.startswith("deadlock") for r in results)
+
+
+def test_wide_catch_up_without_releasing_slots_is_caught():
+    results = [run_wide_pipeline([2, 2, 2], 8, 4, 2, seed, catch_up_commits=False)
+               for seed in range(10)]
+    assert all(r is not None for r in results)

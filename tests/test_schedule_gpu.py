@@ -88,17 +88,19 @@ def test_kernel_followed_the_schedule(M, N, K, variant, plain, column_major):
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "debug build")
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
-def test_watchdog_fires_and_context_survives(variant):
-    # CTA 0's producer never fills pipeline phase 5: the MMA role's wait on it cannot
-    # complete, the 20 ms watchdog must end every role and report TG_ERR_TIMEOUT
+@pytest.mark.parametrize("variant,cta", [(v, 0) for v in VARIANTS] + [("pair", 1), ("wide", 1)])
+def test_watchdog_fires_and_context_survives(variant, cta):
+    # the producer of CTA ``cta`` never fills pipeline phase 5: the MMA role's wait on it cannot
+    # complete, the 20 ms watchdog must end every role and report TG_ERR_TIMEOUT.  In a CTA
+    # pair, CTA 0 (even) skipping leaves a phase that only the odd CTA filled, CTA 1 (odd) one
+    # that only the even CTA armed: the abort path must see both kinds of copies land.
     M, N, K = 512, 512, 1024
     a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=1)
     a_d, b_d = a.cuda(), b.cuda()
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tg.TgError) as e:
         tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
-                                    watchdog_ns=20_000_000, inject_skip_phase=5)
+                                    watchdog_ns=20_000_000, inject_skip_phase=(cta << 32) + 5)
     assert e.value.code == tg.TG_ERR_TIMEOUT
     assert "watchdog" in str(e.value)
     # the context is intact: the status word was cleared and the next GEMM is correct
@@ -195,6 +197,32 @@ def test_group_width_option_followed(M, N, K, variant, group):
                                        trace=trace, group=group) == 0
     want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"], group,
                                     split_tail=True)
+    by_unit = {worker + w * shape["workers"]: (worker, w, bx, by, part)
+               for (worker, w, bx, by, part) in want}
+    got = trace.cpu().numpy()
+    for u in range(units):
+        assert tuple(int(v) for v in got[u]) == by_unit[u], u
+    assert np.array_equal(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"))
+
+
+@pytest.mark.parametrize("M,N,K,rows", [(4096, 4096, 64, "rows"), (2048, 40960, 1024, "columns"),
+                                        (8192, 8192, 4104, "groups")])
+def test_auto_traversal_is_reported_and_followed(M, N, K, rows):
+    # TG_VARIANT_AUTO picks the traversal too: whole rows of tiles when B fits in half of the
+    # L2 (64 MiB), whole columns when only A does, else groups of 8; tg_gemm_launch_shape
+    # reports it and the kernel's trace follows the oracle's enumeration of it
+    shape = tg.tg_gemm_launch_shape(M, N, K)
+    want_order = {"rows": (shape["n_tiles"], 0), "columns": (shape["m_tiles"], 1),
+                  "groups": (8, 0)}[rows]
+    assert (shape["group"], shape["column_major"]) == want_order
+    units = shape["units"]
+    a, b = wl.small_int_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=K)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
+    assert tg.tg_gemm_persistent_debug(a.cuda(), b.cuda(), c, M, N, K, "bf16", trace=trace) == 0
+    want = schedule.enumerate_units(shape["m_tiles"], shape["n_tiles"], shape["workers"],
+                                    shape["group"], split_tail=True,
+                                    column_major=bool(shape["column_major"]))
     by_unit = {worker + w * shape["workers"]: (worker, w, bx, by, part)
                for (worker, w, bx, by, part) in want}
     got = trace.cpu().numpy()
