@@ -547,7 +547,7 @@ def mx_per_config_record(dev, peaks, cores, rows=1024):
     ref = mx.gemm_mxfp8_ref(an[:rows], san[:rows], bn, sbn, "bf16")
     secs = time.perf_counter() - t0
     ok, max_err = gate(wl.bits(c[:rows].cpu()), ref, "bf16")
-    launch = tg.tg_gemm_launch_shape(M, N, K, "pair")
+    launch = tg.tg_gemm_launch_shape(M, N, K, mxfp8=True)
     tflops = flops / (med * 1e-3) / 1e12
     compulsory = M * K + N * K + (M * K + N * K) // 32 + 2 * M * N   # GEMM: A, B, scales, C
     rec = {
@@ -802,11 +802,7 @@ def run_tg_mx(args):
         tg.tg_mxfp8_pack_scales(sb, sb_p, N, K, stream)
         gemm_only()
 
-    launch = tg.tg_gemm_launch_shape(M, N, K, args.variant)   # the GEMM's kernel and launch
-    if launch["variant"] == tg.TG_VARIANT_PAIR_WIDE:
-        # the wide pair kernel is dense-only; where the dense choice is wide, the MXFP8
-        # choice is the pair kernel (its 256 x 256 tiles then fill more than a wave)
-        launch = tg.tg_gemm_launch_shape(M, N, K, "pair")
+    launch = tg.tg_gemm_launch_shape(M, N, K, args.variant, mxfp8=True)   # the GEMM's launch
     kernel = "gemm_mxfp8_pair_ws" if launch["variant"] == tg.TG_VARIANT_PAIR else "gemm_mxfp8_ws"
 
     steps, warm = max(1, args.steps), max(3, args.warmup)

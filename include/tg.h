@@ -69,6 +69,9 @@ enum {
      with 16-byte stores straight from registers (the page's direct C_local_cast store) instead
      of staging it in shared memory for a TMA store (the page's use_tma_store, the default). */
   TG_EPILOGUE_DIRECT = 0x800,
+  /* tg_gemm_launch_shape flag: describe the block-scaled MXFP8 GEMM's launch (tg_gemm_mxfp8*),
+     whose variants are SINGLE and PAIR, instead of the dense GEMM's. */
+  TG_SHAPE_MXFP8 = 0x1000,
   /* tg_tile_schedule_ex flag: apply the tail split (the GEMM does unless TG_SCHEDULE_PLAIN) */
   TG_SCHEDULE_SPLIT_TAIL = 0x1
 };
@@ -179,7 +182,8 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
 /*
  * tg_gemm_launch_shape -- the persistent launch the library would use for an M x N x K
  * dense GEMM on the current device with ``variant`` (TG_VARIANT_* with any TG_SCHEDULE_* flags;
- * AUTO is resolved as tg_gemm_persistent resolves it).
+ * AUTO is resolved as tg_gemm_persistent resolves it), or, with TG_SHAPE_MXFP8, for the
+ * block-scaled MXFP8 GEMM (AUTO resolved as tg_gemm_mxfp8 resolves it; no traversal choice).
  *   *variant_out: the concrete variant; *tile_m, *tile_n: the output tile of one scheduler
  *   worker (256 x 512 for PAIR_WIDE); *m_tiles, *n_tiles: the tile grid; *workers: scheduler
  *   workers (CTAs for SINGLE, CTA pairs for PAIR and PAIR_WIDE); *ctas: CTAs launched;

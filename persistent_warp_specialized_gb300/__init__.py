@@ -31,6 +31,7 @@ TG_SCHEDULE_COLUMN_MAJOR = 0x200
 TG_SCHEDULE_SPLIT_TAIL = 0x1
 TG_SCHEDULE_DYNAMIC = 0x400
 TG_EPILOGUE_DIRECT = 0x800
+TG_SHAPE_MXFP8 = 0x1000
 TG_SCHEDULE_NOALLOC_MAX_UNITS = 65536   # scratch rows of tg_tile_schedule_noalloc
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR,
             "wide": TG_VARIANT_PAIR_WIDE}
@@ -214,13 +215,12 @@ def tg_gemm_config():
 
 
 def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False, dynamic=False,
-                         column_major=False, group=None):
+                         column_major=False, group=None, mxfp8=False):
     """The persistent launch (and traversal) the library uses for M x N x K on the current
-    device."""
+    device: of the dense GEMM, or with ``mxfp8`` of the block-scaled MXFP8 GEMM."""
     vals = [ctypes.c_int() for _ in range(11)]
-    _check(load_library().tg_gemm_launch_shape(
-        M, N, K, _variant(variant, plain, column_major, dynamic, group),
-        *[ctypes.byref(v) for v in vals]))
+    code = _variant(variant, plain, column_major, dynamic, group) | (TG_SHAPE_MXFP8 if mxfp8 else 0)
+    _check(load_library().tg_gemm_launch_shape(M, N, K, code, *[ctypes.byref(v) for v in vals]))
     keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas",
             "split_from", "units", "group", "column_major")
     return dict(zip(keys, (v.value for v in vals)))

@@ -571,18 +571,23 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
                          int* ctas, int* split_from, int* units, int* group,
                          int* column_major) {
+  const bool mxfp8 = (variant & TG_SHAPE_MXFP8) != 0;
+  variant &= ~TG_SHAPE_MXFP8;
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
-  const bool choose_traversal = auto_traversal(variant);
+  const bool choose_traversal = auto_traversal(variant) && !mxfp8;
   Raster r = {group_of(variant), (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u};
   variant &= ~kScheduleFlags;
+  if (mxfp8 && (dynamic || variant == TG_VARIANT_PAIR_WIDE))
+    return fail(TG_ERR_ARG, "the MXFP8 GEMM has the single and pair variants only");
   if (M < 1 || N < 1 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return fail(TG_ERR_ARG, "sizes must be M, N in [1, 2^31), K in [0, 2^31)");
   int sms = 0, max_pairs = 0;
   int rc = device_ready(&sms, &max_pairs);
   if (rc != TG_OK) return rc;
-  if (variant == TG_VARIANT_AUTO) variant = auto_variant_dense(M, N, K, max_pairs);
+  if (variant == TG_VARIANT_AUTO)
+    variant = mxfp8 ? auto_variant(M, N, K, max_pairs) : auto_variant_dense(M, N, K, max_pairs);
   if (dynamic && variant != TG_VARIANT_SINGLE)
     return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
   const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);

@@ -139,7 +139,7 @@ def test_scales_span_the_e8m0_range(variant):
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4000, 7000, 128), (256, 256, 256),
                                    (8192, 8192, 128)])
 def test_kernel_followed_the_schedule(M, N, K, plain, column_major, variant):
-    shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain)
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant, plain, mxfp8=True)
     units = shape["units"]
     trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=5)
@@ -201,7 +201,7 @@ def test_full_size_workload_sampled_entries(variant):
 @pytest.mark.parametrize("variant", MX_VARIANTS)
 def test_group_width_option_followed(variant):
     M, N, K, group = 4096, 4096, 128, 12
-    shape = tg.tg_gemm_launch_shape(M, N, K, variant)
+    shape = tg.tg_gemm_launch_shape(M, N, K, variant, mxfp8=True)
     units = shape["units"]
     trace = torch.full((units, 5), -7, dtype=torch.int32, device="cuda")
     a, sa, b, sb = wl.mx_int_inputs(M, N, K, seed=12)

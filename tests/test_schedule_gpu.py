@@ -88,19 +88,23 @@ def test_kernel_followed_the_schedule(M, N, K, variant, plain, column_major):
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "bf16"), "bf16", "debug build")
 
 
-@pytest.mark.parametrize("variant,cta", [(v, 0) for v in VARIANTS] + [("pair", 1), ("wide", 1)])
-def test_watchdog_fires_and_context_survives(variant, cta):
-    # the producer of CTA ``cta`` never fills pipeline phase 5: the MMA role's wait on it cannot
+@pytest.mark.parametrize("variant,cta,plain", [(v, 0, False) for v in VARIANTS] +
+                         [("pair", 1, False), ("wide", 1, False), ("pair", 0, True),
+                          ("pair", 1, True)])
+def test_watchdog_fires_and_context_survives(variant, cta, plain):
+    # the producer of CTA ``cta`` never fills pipeline phase 1: the MMA role's wait on it cannot
     # complete, the 20 ms watchdog must end every role and report TG_ERR_TIMEOUT.  In a CTA
     # pair, CTA 0 (even) skipping leaves a phase that only the odd CTA filled, CTA 1 (odd) one
-    # that only the even CTA armed: the abort path must see both kinds of copies land.
+    # that only the even CTA armed: the abort path must see both kinds of copies land.  With
+    # ``plain`` the pair kernel runs the 2 x 2 tiles whole instead of as half-width units.
     M, N, K = 512, 512, 1024
     a, b = wl.make_inputs(M, N, K, "bf16", "uniform", seed=1)
     a_d, b_d = a.cuda(), b.cuda()
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tg.TgError) as e:
         tg.tg_gemm_persistent_debug(a_d, b_d, c, M, N, K, "bf16", variant=variant,
-                                    watchdog_ns=20_000_000, inject_skip_phase=(cta << 32) + 5)
+                                    watchdog_ns=20_000_000, inject_skip_phase=(cta << 32) + 1,
+                                    plain=plain)
     assert e.value.code == tg.TG_ERR_TIMEOUT
     assert "watchdog" in str(e.value)
     # the context is intact: the status word was cleared and the next GEMM is correct
