@@ -95,9 +95,9 @@ enum {
  *   A_dev [M, K], B_dev [K, N], C_dev [M, N]; all of type ``dtype`` (TG_F16 or TG_BF16).
  *   M, N, K >= 0 and < 2^31.  N % 8 == 0 and K % 8 == 0.  All three pointers 16-byte aligned.
  *   C must not overlap A or B.  M == 0 or N == 0: nothing is done.  K == 0: C is zero-filled.
- * Persistent kernels walk the output tiles in grouped order (group 8; see tg_tile_schedule):
- * one CTA per SM on 128 x 256 tiles, or one CTA pair per two SMs on 256 x 256 or 256 x 512
- * tiles, chosen as TG_VARIANT_AUTO describes at tg_gemm_persistent_ex.  Partial edge tiles in
+ * Persistent kernels walk the output tiles in grouped order (see tg_tile_schedule): one CTA
+ * per SM on 128 x 256 tiles, or one CTA pair per two SMs on 256 x 256 or 256 x 512 tiles, with
+ * the kernel and the traversal chosen as TG_VARIANT_AUTO describes at tg_gemm_persistent_ex.  Partial edge tiles in
  * M and N and a partial last k-block are handled inside the kernel (zero-filled loads,
  * clipped stores).
  */
@@ -109,8 +109,12 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
  * Same arguments, rules and results; TG_ERR_ARG for an unknown variant.  The pair variant
  * walks ceil(M/256) x ceil(N/256) tiles with one scheduler worker per CTA pair, the wide pair
  * variant ceil(M/256) x ceil(N/512) tiles (its tail-split half units are 256 x 256).
- * TG_VARIANT_AUTO takes the wide pair variant when its tiles fill at least four waves of
- * resident pairs, else the pair variant when its tiles fill at least one, else the single one.
+ * TG_VARIANT_AUTO takes the wide pair variant when its tiles fill at least one wave of resident
+ * pairs and K >= 6144, or four waves and K >= 4096; else the pair variant when its tiles fill at
+ * least one wave; else the single one.  Unless the variant carries TG_SCHEDULE_PLAIN,
+ * TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP, AUTO also picks the traversal: whole rows of
+ * tiles when all of B fits in 64 MiB (half of the L2), whole columns when only A does, else
+ * groups of 8 in row order (tg_gemm_launch_shape reports the choice).
  */
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
                           int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant);
