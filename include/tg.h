@@ -114,7 +114,8 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
  * least one wave; else the single one.  Unless the variant carries TG_SCHEDULE_PLAIN,
  * TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP, AUTO also picks the traversal: whole rows of
  * tiles when all of B fits in 64 MiB (half of the L2), whole columns when only A does, else
- * groups of 8 in row order (tg_gemm_launch_shape reports the choice).
+ * groups of 8 in row order, or for the wide pair variant groups of round(sqrt(2 x workers))
+ * M-tiles in column order (tg_gemm_launch_shape reports the choice).
  */
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
                           int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant);
@@ -194,9 +195,8 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
  *   *split_from, *units: the tail split (units below split_from are whole tiles;
  *   split_from == units: no split); *group, *column_major: the traversal (the grouped order's
  *   width and whether it runs along M first).  With TG_VARIANT_AUTO and no TG_SCHEDULE_PLAIN,
- *   TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP flag, the library also picks the traversal:
- *   whole rows of tiles when all of B fits in half of the L2 (64 MiB), whole columns when only
- *   A does, else groups of 8 in row order.  Any pointer may be NULL.
+ *   TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP flag, the library also picks the traversal,
+ *   as tg_gemm_persistent_ex describes.  Any pointer may be NULL.
  * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
  */
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,

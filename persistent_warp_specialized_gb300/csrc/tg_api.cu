@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -212,20 +213,31 @@ bool pair_variant(int v) { return v == TG_VARIANT_PAIR || v == TG_VARIANT_PAIR_W
 // an order nor a group width (the page's scheduler options ``column_major`` and
 // ``swizzle_size``).  When all of B fits in half of the L2, whole rows of tiles (group = the
 // number of N-tiles) read each row slab of A from DRAM once while B stays resident; when only A
-// fits, whole columns do the same with the roles exchanged; otherwise the page's grouped order
-// of width 8.  Measured on GB300 (CTA-pair kernel, medians of 3 rounds): 4096^3 rows 1797 vs
-// groups of 8 1745 TFLOP/s, 4000 x 7000 x 2048 rows of 16 1637 vs 1612; at 8192^3 (B 128 MiB)
-// groups of 8 stay best.
+// fits, whole columns do the same with the roles exchanged.  Otherwise a wave of P tiles covers
+// a block of them, and the operand bytes it touches (its A rows plus its B columns) are least
+// when both extents match: about sqrt(P tile_n / tile_m) M-tiles by sqrt(P tile_m / tile_n)
+// N-tiles.  For the square 256 x 256 pair tiles (P = 76) that is the page's group of 8 (row
+// order); for the wide pair kernel's 256 x 512 tiles it is groups of 12 M-tiles in column order.
+// Measured on GB300 (medians of alternating rounds, TFLOP/s): pair kernel 4096^3 rows 1797 vs
+// groups of 8 1745, 4000 x 7000 x 2048 rows of 16 1637 vs 1612, 8192^3 groups of 8 best; wide
+// kernel, column order groups of 12 vs row order groups of 8: 8192^3 1959 vs 1944 (3000
+// back-to-back launches: 1741 vs 1716), 6144^3 1924 vs 1908, 8192 x 8192 x 16384 2009 vs 1986.
 struct Raster {
   uint32_t group, column_major;
 };
 constexpr uint64_t kHalfL2Bytes = 64ull << 20;
 
-Raster auto_raster(int64_t M, int64_t N, int64_t K, uint32_t m_tiles, uint32_t n_tiles) {
+Raster auto_raster(int64_t M, int64_t N, int64_t K, uint32_t m_tiles, uint32_t n_tiles,
+                   uint32_t tile_m, uint32_t tile_n, uint32_t workers) {
   const uint64_t a_bytes = uint64_t(M) * K * tg::kElemBytes;
   const uint64_t b_bytes = uint64_t(K) * N * tg::kElemBytes;
   if (b_bytes <= kHalfL2Bytes) return {n_tiles < 255u ? n_tiles : 255u, 0u};
   if (a_bytes <= kHalfL2Bytes) return {m_tiles < 255u ? m_tiles : 255u, 1u};
+  if (tile_n > tile_m) {   // wide tiles: panels of M-tiles, as many as balance the wave
+    const double g = std::sqrt(double(workers) * tile_n / tile_m);
+    const uint32_t gi = static_cast<uint32_t>(g + 0.5);
+    return {gi < 1u ? 1u : (gi > 255u ? 255u : gi), 1u};
+  }
   return {static_cast<uint32_t>(tg::kGroup), 0u};
 }
 
@@ -319,7 +331,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.K = static_cast<uint32_t>(K);
   const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
   if (choose_traversal) {
-    const Raster r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles);
+    const Raster r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles, sh.tile_m, sh.tile_n,
+                                 sh.workers);
     group = r.group;
     column_major = r.column_major;
   }
@@ -591,7 +604,8 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
   if (dynamic && variant != TG_VARIANT_SINGLE)
     return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
   const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
-  if (choose_traversal) r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles);
+  if (choose_traversal)
+    r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles, sh.tile_m, sh.tile_n, sh.workers);
   if (variant_out) *variant_out = variant;
   if (group) *group = static_cast<int>(r.group);
   if (column_major) *column_major = static_cast<int>(r.column_major);

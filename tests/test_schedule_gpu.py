@@ -3,6 +3,7 @@ the GEMM kernel's own trace against the same enumeration, and the watchdog.
 """
 
 import itertools
+import math
 import os
 
 import numpy as np
@@ -213,11 +214,15 @@ def test_group_width_option_followed(M, N, K, variant, group):
                                         (8192, 8192, 4104, "groups")])
 def test_auto_traversal_is_reported_and_followed(M, N, K, rows):
     # TG_VARIANT_AUTO picks the traversal too: whole rows of tiles when B fits in half of the
-    # L2 (64 MiB), whole columns when only A does, else groups of 8; tg_gemm_launch_shape
+    # L2 (64 MiB), whole columns when only A does, else balanced groups; tg_gemm_launch_shape
     # reports it and the kernel's trace follows the oracle's enumeration of it
     shape = tg.tg_gemm_launch_shape(M, N, K)
+    # "groups": neither operand fits; the wide kernel's 256 x 512 tiles take groups of
+    # round(sqrt(2 P)) M-tiles in column order, square tiles the page's 8 in row order
+    wide = shape["tile_n"] > shape["tile_m"]
+    groups = (int(math.sqrt(2 * shape["workers"]) + 0.5), 1) if wide else (8, 0)
     want_order = {"rows": (shape["n_tiles"], 0), "columns": (shape["m_tiles"], 1),
-                  "groups": (8, 0)}[rows]
+                  "groups": groups}[rows]
     assert (shape["group"], shape["column_major"]) == want_order
     units = shape["units"]
     a, b = wl.small_int_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=K)
