@@ -175,8 +175,12 @@ __device__ __forceinline__ void epilogue_store_packed(const uint32_t (&pk)[32], 
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-      if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N))
-        tma_store_2d(tmC, sbuf, x, row0);
+      if (row0 < static_cast<int32_t>(p.M) && x < static_cast<int32_t>(p.N)) {
+        if (kCPolicy != 0)
+          tma_store_2d_hint(tmC, sbuf, x, row0, l2_policy<kCPolicy>());
+        else
+          tma_store_2d(tmC, sbuf, x, row0);
+      }
       bulk_commit_group();   // one group per chunk, empty when the chunk is outside C
     }
   }
