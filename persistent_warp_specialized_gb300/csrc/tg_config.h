@@ -176,14 +176,27 @@ constexpr int kMxPairStages = TG_MX_PAIR_STAGES;
 constexpr uint32_t kMxPairBBytes = (kBN / 2) * kMxBK;              // 16 KiB: 128 rows of B
 constexpr uint32_t kMxPairKbBytes = kMxABytes + kMxPairBBytes;     // 32 KiB per k-block
 constexpr uint32_t kMxPairStageBytes = kMxPairKB * kMxPairKbBytes;  // A blocks, then B blocks
-constexpr uint32_t kMxPairTxBytes = 2 * kMxPairKB * (kMxPairKbBytes + kMxAtomSetBytes);
+constexpr uint32_t kMxPairTxBytes = 2 * kMxPairKB * kMxPairKbBytes;   // A, B of both CTAs
+constexpr uint32_t kMxPairSfTxBytes = kMxPairKB * kMxAtomSetBytes;     // one CTA's atoms
+// The scale atoms run TG_MX_PAIR_SF_AHEAD stages ahead of the operands through a ring of their
+// own (shared-memory atom sets and TMEM scale slots): stage p's atoms are loaded together with
+// the operands of stage p - ahead, so the epilogue warps that write them into TMEM have
+// ahead + S - 1 stages of MMA time to do it.  Measured on GB300 (MXFP8 GEMM TFLOP/s, two
+// alternating rounds; 8192^3 / 6144^3 / 4096^3): ahead 1: 3423 / 3294 / 2897, ahead 2: 3408 /
+// 3281 / 2870; one k-block per stage (6 stages), ahead 2: 2937 / 2805 / 2346, ahead 4: 2820.
+#ifndef TG_MX_PAIR_SF_AHEAD
+#define TG_MX_PAIR_SF_AHEAD 1
+#endif
+constexpr int kMxPairSfAhead = TG_MX_PAIR_SF_AHEAD;
+constexpr int kMxPairSfSlots = kMxPairStages + kMxPairSfAhead;      // stages in the scale ring
 constexpr uint32_t kMxPairAtomRegionBytes =
-    (kMxPairStages * kMxPairKB * kMxAtomSetBytes + 1023u) & ~1023u;
+    (kMxPairSfSlots * kMxPairKB * kMxAtomSetBytes + 1023u) & ~1023u;
 constexpr uint32_t kMxPairSmemBytes = kSmemAlignSlack + kMxPairStages * kMxPairStageBytes +
                                       kMxPairAtomRegionBytes + kMxEpiSmemBytes;
 static_assert(kMxPairSmemBytes + 512 <= 232448, "shared memory per CTA (MXFP8 pair)");
-static_assert(kMxAccCols + kMxPairStages * kMxPairKB * kMxSfColsPerStage <= kTmemCols,
+static_assert(kMxAccCols + kMxPairSfSlots * kMxPairKB * kMxSfColsPerStage <= kTmemCols,
               "MXFP8 pair TMEM budget");
+static_assert(kMxPairSfSlots <= 32, "atom slots tracked in one 32-bit mask");
 
 // watchdog: bits of the per-device status word naming the role that gave up a wait
 constexpr uint32_t kRoleProducer = 1u;

@@ -19,7 +19,7 @@
 // rows 0..127 and B columns 0..127 from the even CTA's slot and the rest from the odd
 // CTA's slot at the same offset, and writes 128 rows into each CTA's TMEM.  tcgen05.commit
 // with a CTA mask of 0b11 completes ``consumed[s]`` and ``tmem_full[w & 1]`` in both CTAs.
-// Both CTAs' epilogues arrive on the even CTA's ``tmem_empty[w & 1]`` (count 256).
+// Both CTAs' epilogue warps report on the even CTA's ``tmem_empty[w & 1]`` (pair_report_warp).
 //
 // All tcgen05 instructions of this kernel use cta_group::2.  Waits are bounded exactly as in
 // the single-CTA kernel; an abort also raises the peer CTA's flag, and the pair meets at a
@@ -46,10 +46,11 @@ struct __align__(8) PairCtl {
   uint64_t loaded[kPairStages];      // used in the even CTA only
   uint64_t consumed[kPairStages];
   uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];            // used in the even CTA only (count 256)
+  uint64_t tmem_empty[2];            // used in the even CTA only (see pair_report_warp)
   uint64_t drain;
   uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
   PairFills<kPairStages> fills;
+  uint32_t sink[kEpiWarps];          // even CTA: target of the odd epilogue warps' st.async
   uint32_t tmem_base;
   int abort;
 };
@@ -58,17 +59,22 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-// Like wait_or_abort, but a timeout also raises the peer CTA's abort flag.
+// Like wait_or_abort, but a timeout also raises the peer CTA's abort flag.  CLUSTER: acquire
+// at cluster scope, for a phase that the peer CTA's threads complete with release semantics.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity,
                                                    volatile int* abort_flag,
                                                    uint32_t peer_abort_addr, uint64_t limit_ns,
                                                    uint32_t role) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto ready = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (ready()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (ready()) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -76,6 +82,25 @@ __device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity
       atomicOr(&g_watchdog_status, role);
       return false;
     }
+  }
+}
+
+// One epilogue warp reports to the pair's MMA thread on the even CTA's barrier ``bar`` (its
+// shared::cta address; initialised with a count of kEpiWarps): the warp has finished its
+// tcgen05 accesses and fenced them (tcgen05.fence::before_thread_sync).  Lane 0 reports for the
+// warp: in the even CTA an arrive that expects 4 transaction bytes, in the odd CTA a 4-byte
+// st.async to ``sink_even`` (an unused word of the even CTA) that completes them with release
+// semantics at cluster scope.  The waiter acquires at cluster scope.  One report per warp,
+// and st.async rather than a release-arrive on the peer's barrier, which held the warp for
+// about 1250 cycles.
+__device__ __forceinline__ void pair_report_warp(uint32_t bar, uint32_t rank, uint32_t lane,
+                                                 uint32_t sink_even) {
+  __syncwarp();
+  if (lane == 0) {
+    if (rank == 0)
+      mbar_arrive_expect_tx(bar, 4);
+    else
+      st_async_u32(sink_even, 0u, mapa_shared(bar, 0));
   }
 }
 
@@ -162,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tmem_full + 8u * b, 1);
-      mbar_init(bar_tmem_empty + 8u * b, 2 * kEpiThreads);
+      mbar_init(bar_tmem_empty + 8u * b, kEpiWarps);
     }
     mbar_init(bar_drain, 1);
     mbar_init(smem_u32(&ctl.odd_done), 1);
@@ -269,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && sched.valid()) {
         const uint32_t w = sched.current_iter;
         const uint32_t buf = w & 1u;
-        if (!pair_wait_or_abort(bar_tmem_empty + 8u * buf, ((w >> 1) & 1u) ^ 1u, abort_flag,
+        if (!pair_wait_or_abort<true>(bar_tmem_empty + 8u * buf, ((w >> 1) & 1u) ^ 1u, abort_flag,
                                 peer_abort, limit, kRoleMma)) {
           ok = false;
           break;
@@ -310,6 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t q = warp - kFirstEpiWarp;
+    const uint32_t sink_even = mapa_shared(smem_u32(&ctl.sink[q]), 0);
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
                                     p.total_units, p.column_major);
     sched.init(pair);
@@ -333,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
         if (j == chunks - 1) {
           tcgen05_fence_before_sync();
-          mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * buf, 0));
+          pair_report_warp(bar_tmem_empty + 8u * buf, rank, lane, sink_even);
         }
         const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
         epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,

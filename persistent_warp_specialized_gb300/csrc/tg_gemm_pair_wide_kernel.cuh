@@ -34,10 +34,11 @@ struct __align__(8) WideCtl {
   uint64_t loaded[kWideStages];      // used in the even CTA only
   uint64_t consumed[kWideStages];
   uint64_t tmem_full;
-  uint64_t tmem_empty[2];            // per N-half; used in the even CTA only (count 256)
+  uint64_t tmem_empty[2];            // per N-half; used in the even CTA only (pair_report_warp)
   uint64_t drain;
   uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
   PairFills<kWideStages> fills;
+  uint32_t sink[kEpiWarps];          // even CTA: target of the odd epilogue warps' st.async
   uint32_t tmem_base;
   int abort;
 };
@@ -74,8 +75,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_consumed + 8u * s, 1);
     }
     mbar_init(bar_tmem_full, 1);
-    mbar_init(bar_tmem_empty, 2 * kEpiThreads);
-    mbar_init(bar_tmem_empty + 8u, 2 * kEpiThreads);
+    mbar_init(bar_tmem_empty, kEpiWarps);
+    mbar_init(bar_tmem_empty + 8u, kEpiWarps);
     mbar_init(bar_drain, 1);
     mbar_init(smem_u32(&ctl.odd_done), 1);
 #pragma unroll
@@ -196,7 +197,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tcgen05_fence_after_sync();
           if (k == 0) {
             // half 0 of the previous unit's accumulator has been read out by both epilogues
-            if (!pair_wait_or_abort(bar_tmem_empty, (w & 1u) ^ 1u, abort_flag, peer_abort,
+            if (!pair_wait_or_abort<true>(bar_tmem_empty, (w & 1u) ^ 1u, abort_flag, peer_abort,
                                     limit, kRoleMma)) {
               ok = false;
               break;
@@ -210,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (k < defer) continue;   // slot s stays held until half 1 has read it
           if (k == defer) {
-            if (!pair_wait_or_abort(bar_tmem_empty + 8u, (w & 1u) ^ 1u, abort_flag, peer_abort,
+            if (!pair_wait_or_abort<true>(bar_tmem_empty + 8u, (w & 1u) ^ 1u, abort_flag, peer_abort,
                                     limit, kRoleMma)) {
               ok = false;
               break;
@@ -236,6 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const uint32_t q = warp - kFirstEpiWarp;
+    const uint32_t sink_even = mapa_shared(smem_u32(&ctl.sink[q]), 0);
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
                                   p.total_units, p.column_major);
     sched.init(pair);
@@ -255,7 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (uint32_t h = 0; h < 2; ++h) {
         if (h >= halves) {
           tcgen05_fence_before_sync();
-          mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));   // unused half
+          pair_report_warp(bar_tmem_empty + 8u * h, rank, lane, sink_even);   // unused half
           continue;
         }
         // the whole N-half into registers, converted (4 chunks x 32 words per lane), then
@@ -268,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pack_chunk<DT>(v, pk[j]);
         }
         tcgen05_fence_before_sync();
-        mbar_arrive_cluster(mapa_shared(bar_tmem_empty + 8u * h, 0));
+        pair_report_warp(bar_tmem_empty + 8u * h, rank, lane, sink_even);
 #pragma unroll
         for (uint32_t j = 0; j < kBN / kEpiN; ++j, ++chunk) {
           const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;

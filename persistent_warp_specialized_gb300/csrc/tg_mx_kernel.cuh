@@ -71,7 +71,12 @@ __device__ __forceinline__ void mx_store_chunk(const uint32_t (&w)[32], uint32_t
   fence_proxy_async_shared();
   __syncwarp();
   if (lane == 0) {
-    if (row0 < static_cast<int32_t>(M) && x < static_cast<int32_t>(N)) tma_store_2d(tmC, sbuf, x, row0);
+    if (row0 < static_cast<int32_t>(M) && x < static_cast<int32_t>(N)) {
+      if (kCPolicy != 0)
+        tma_store_2d_hint(tmC, sbuf, x, row0, l2_policy<kCPolicy>());
+      else
+        tma_store_2d(tmC, sbuf, x, row0);
+    }
     bulk_commit_group();
   }
   __syncwarp();

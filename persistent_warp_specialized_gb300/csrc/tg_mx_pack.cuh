@@ -3,7 +3,8 @@
 // Row-major E8M0 scales sf [rows, 4 * k_blocks] become atoms: out[(k * row_blocks + b) * 512 +
 // (r % 32) * 16 + (r / 32) * 4 + j] = sf[b * 128 + r, 4 k + j] (0 for rows >= rows), for every
 // k-block k, row block b and r < 128 -- the source layout of tcgen05.cp .32x128b.warpx4 (see
-// tg_mx_kernel.cuh).  A block takes 128 rows x 8 k-blocks: it reads each row's 32 bytes (eight
+// tg_mx_kernel.cuh; the CTA-pair kernel's epilogue warps read it one 16-byte row per lane and
+// write it with tcgen05.st).  A block takes 128 rows x 8 k-blocks: it reads each row's 32 bytes (eight
 // 4-byte words, neighbouring threads on neighbouring words), reorders them in shared memory,
 // and writes the eight 512-byte atoms with neighbouring threads on neighbouring words.
 #pragma once

@@ -61,6 +61,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but returns at once (mbarrier.test_wait): for a thread that polls several
+// barriers in turn.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, with acquire semantics at cluster scope: writes that another CTA of the
 // cluster made before its release-arrive on ``bar`` are visible once this returns true.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -265,6 +279,31 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// Warp-collective registers -> TMEM: lane i of the warp writes TMEM lane (taddr.lane + i),
+// 16 consecutive 32-bit columns starting at taddr.col.  Asynchronous: tcgen05_wait_st makes
+// the warp's writes complete.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tcgen05_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                             uint32_t& d) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- block-scaled MMA (MXFP8)
 // Contiguous global -> shared copy of ``bytes`` (a multiple of 16; both addresses 16-byte
 // aligned) by the bulk-copy engine, completing ``bytes`` transaction bytes on ``bar``.
@@ -281,13 +320,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Issued by one thread; ordered before tcgen05.mma issued later by the same thread.
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-
-// The pair form: issued by the even CTA, copies each CTA's atom at ``sdesc`` into that CTA's
-// own TMEM at ``taddr`` (measured on GB300), replicated into its four lane quadrants.
-__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
 
@@ -381,6 +413,19 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// Asynchronous 4-byte store into the shared memory of another CTA of the cluster (both
+// addresses shared::cluster) that counts 4 transaction bytes on an mbarrier of that CTA.  The
+// issuing thread does not wait for it; its complete_tx has release semantics at cluster scope,
+// so what this thread ordered before it is visible to a thread that acquires the barrier's phase.
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(v), "r"(cluster_bar)
+      : "memory");
 }
 
 // 2-D tiled load into this CTA's shared memory whose byte count completes on an mbarrier that

@@ -361,6 +361,167 @@ def test_mx_scales_arriving_on_loaded_are_caught():
     assert any(f is not None for f in failures)
 
 
+# ---------------------------------------------------------------- MXFP8 pair: scales by the epilogue
+# The CTA-pair MXFP8 kernel (tg_mx_pair_kernel.cuh) writes the TMEM scale slots from its
+# epilogue warps, through a scale ring of A = S + D slots that runs D phases ahead of the
+# operand ring.  The producer loads the atoms of phases 0 .. D - 1 first; then per phase p it
+# waits consumed[p % S] (parity ((p // S) & 1) ^ 1), loads the atoms of phase p + D into scale
+# slot (p + D) % A (arming sf_loaded of that slot) and the operands of p (arming loaded[s]);
+# the bytes land later in any order.  The MMA role waits tmem_empty with parity (w & 1) ^ 1
+# before unit w (one accumulator), then per phase loaded[p % S] (parity (p // S) & 1) and
+# sf_ready[p % A] (parity (p // A) & 1), and commits consumed[p % S]; after the unit's last
+# phase it completes tmem_full.  The epilogue is one sequential agent: it polls, draining unit
+# w once tmem_full passes with parity w & 1 and otherwise writing the scale slot of its next
+# phase q once sf_loaded[q % A] passes with parity (q // A) & 1; after a drain it arrives on
+# tmem_empty and stores four chunks, trying one scale slot before each chunk after the first.
+# ``polling=False`` is the design that waits for tmem_full before writing any slot of the
+# unit: it deadlocks.  ``slots`` below S + D lets a load overwrite atoms or a TMEM slot that is
+# still in use.
+
+
+def run_mx_pair_epilogue(S, k_stages, units, seed, D=2, polling=True, slots=None):
+    rng = random.Random(seed)
+    A = S + D if slots is None else slots
+    consumed = [Barrier() for _ in range(S)]
+    loaded = [TxBarrier(1) for _ in range(S)]
+    sf_loaded = [TxBarrier(1) for _ in range(A)]
+    sf_ready = [Barrier() for _ in range(A)]
+    tmem_full, tmem_empty = Barrier(), Barrier()
+    total = units * k_stages
+    stage = [None] * S       # phase whose operands sit in ring slot s
+    atoms = [None] * A       # phase whose atoms sit in shared-memory scale slot a
+    slot = [None] * A        # phase whose scales sit in TMEM scale slot a
+    in_flight = []           # (what, slot, phase) loads not landed yet
+    prod = mma = ps = wd = 0
+    sf_next = 0              # phase whose atoms the producer loads next
+    entered = False          # the MMA role has passed tmem_empty for its current unit
+    acc = None               # unit whose finished sum the accumulator holds
+    chunks = 0               # chunks of the drained unit still to store
+
+    def load_atoms():
+        nonlocal sf_next
+        if sf_next >= total:
+            return None
+        a = sf_next % A
+        if sf_loaded[a].arrive(expect_tx=1, armed=True) == "early":
+            return f"sf_loaded[{a}] completed before phase {sf_next} was armed"
+        in_flight.append(("sf", a, sf_next))
+        sf_next += 1
+        return None
+
+    def write_scale():
+        nonlocal ps
+        a = ps % A
+        if atoms[a] != ps:
+            return f"scale slot of phase {ps} written from the atoms of phase {atoms[a]}"
+        if slot[a] is not None and mma <= slot[a]:
+            return f"scale slot {a} rewritten (phase {ps}) before phase {slot[a]} was consumed"
+        slot[a] = ps
+        sf_ready[a].complete()
+        ps += 1
+        return None
+
+    def scale_ready():
+        return ps < total and sf_loaded[ps % A].passes((ps // A) & 1)
+
+    for _ in range(D):
+        err = load_atoms()
+        if err:
+            return err
+    while wd < units:
+        moves = []
+        if prod < total and consumed[prod % S].passes(((prod // S) & 1) ^ 1):
+            moves.append("p")
+        if in_flight:
+            moves.append("land")
+        if mma < total:
+            w, s, a = mma // k_stages, mma % S, mma % A
+            if mma % k_stages == 0 and not entered:
+                if tmem_empty.passes((w & 1) ^ 1):
+                    moves.append("m")
+            elif loaded[s].passes((mma // S) & 1) and sf_ready[a].passes((mma // A) & 1):
+                moves.append("m")
+        if chunks:
+            moves.append("e")
+        elif tmem_full.passes(wd & 1) or (polling and scale_ready()):
+            moves.append("e")
+        if not moves:
+            return f"deadlock: producer {prod}, scales {ps}, mma {mma}, drain {wd}"
+        mv = rng.choice(moves)
+        if mv == "p":
+            s = prod % S
+            err = load_atoms()
+            if err:
+                return err
+            if loaded[s].arrive(expect_tx=1, armed=True) == "early":
+                return f"loaded[{s}] completed before phase {prod} was armed"
+            in_flight.append(("op", s, prod))
+            prod += 1
+        elif mv == "land":
+            what, s, ph = in_flight.pop(rng.randrange(len(in_flight)))
+            if what == "op":
+                stage[s] = ph
+                done = loaded[s].land(1)
+            else:
+                if atoms[s] is not None and ps <= atoms[s]:
+                    return f"atoms of phase {atoms[s]} overwritten before they were read"
+                atoms[s] = ph
+                done = sf_loaded[s].land(1)
+            if done == "early":
+                return f"{what}[{s}] completed early (phase {ph})"
+        elif mv == "m":
+            w, s, a = mma // k_stages, mma % S, mma % A
+            if mma % k_stages == 0 and not entered:
+                entered = True
+                continue
+            if stage[s] != mma:
+                return f"MMA phase {mma} read the operands of phase {stage[s]}"
+            if slot[a] != mma:
+                return f"MMA phase {mma} read the scales of phase {slot[a]}"
+            consumed[s].complete()
+            mma += 1
+            if mma % k_stages == 0:
+                acc = w
+                entered = False
+                tmem_full.complete()
+        elif chunks:
+            if chunks < 4 and scale_ready():
+                err = write_scale()
+                if err:
+                    return err
+            chunks -= 1
+            if chunks == 0:
+                wd += 1
+        elif tmem_full.passes(wd & 1):
+            if acc != wd:
+                return f"drain of unit {wd} read the accumulator of unit {acc}"
+            tmem_empty.complete()
+            chunks = 4
+        else:
+            err = write_scale()
+            if err:
+                return err
+    return None
+
+
+@pytest.mark.parametrize("S,D,k_stages", [(3, 2, 1), (3, 2, 2), (3, 2, 5), (3, 0, 3), (2, 3, 3),
+                                          (4, 1, 7)])
+def test_mx_pair_epilogue_scale_path_holds(S, D, k_stages):
+    for seed in range(150):
+        assert run_mx_pair_epilogue(S, k_stages, 6, seed, D=D) is None, (S, D, k_stages, seed)
+
+
+def test_mx_pair_scales_written_only_after_the_drain_deadlock():
+    assert run_mx_pair_epilogue(3, 4, 3, 0, polling=False).startswith("deadlock")
+
+
+def test_mx_pair_scale_ring_shorter_than_operands_plus_lead_is_caught():
+    # with A = S + D - 1 slots, loading phase p + D's atoms after consumed of p - S reuses the
+    # slot of phase p - S + 1, which may not have been read yet
+    failures = [run_mx_pair_epilogue(3, 4, 4, seed, D=2, slots=4) for seed in range(150)]
+    assert any(f is not None and "deadlock" not in f for f in failures)
+
+
 # ---------------------------------------------------------------- wide pair accumulator
 # The wide pair kernel (tg_gemm_pair_wide_kernel.cuh) has one accumulator made of two N-halves
 # (TMEM columns 0..255 and 256..511) in each CTA of the pair.  The MMA role (even CTA) writes
