@@ -112,3 +112,90 @@ def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True, col
             rows.append((c, w, bx, by, part))
             w += 1
     return rows
+
+
+# ---------------------------------------------------------------- stream-K tail
+# Reading beyond the pages (their scheduler walks whole tiles): the library can instead split
+# the last partial wave along K.  With T tiles and P workers, the R = T mod P tiles that come
+# last in the traversal form the tail; their k-blocks, numbered tile-major (tile i of the tail
+# owns numbers i*KB .. i*KB + KB - 1), are cut into P contiguous ranges, worker c taking
+# [floor(c*R*KB/P), floor((c+1)*R*KB/P)).  The whole tiles before the tail keep the grid stride.
+# A worker's range is shorter than KB (R < P), so it meets at most two tail tiles.  The worker
+# whose range holds a tail tile's last k-block owns that tile: it adds the other workers' partial
+# sums of the tile to its own and stores the tile.  A worker walks its part of the later tile
+# (a contribution) before its part of the earlier one (which it owns), so every owner waits only
+# for lower-numbered workers' contributions, each made first in its worker's range.
+
+
+def streamk_applies(tiles, workers, k_blocks):
+    """The library's rule for taking the stream-K tail when a workspace is given: the partial
+    wave holds between a quarter of a wave (a tail tile then has about four contributors at
+    most) and four fifths of one (above that a whole last wave costs less than a fifth of a
+    tile's time more than the tail's work, about what the partial sums' round trip costs), and
+    every worker gets at least eight k-blocks of it."""
+    rem = tiles % workers
+    return rem > 0 and 4 * rem >= workers and 5 * rem <= 4 * workers and rem * k_blocks >= 8 * workers
+
+
+def streamk_range(c, workers, sk_tiles, k_blocks):
+    """Worker c's k-blocks [lo, hi) of the tail, tile-major."""
+    total = sk_tiles * k_blocks
+    return total * c // workers, total * (c + 1) // workers
+
+
+def streamk_segments(c, workers, sk_tiles, k_blocks):
+    """Worker c's tail segments in the order it walks them: (tail tile index, k_lo, k_hi, owns).
+    Brute force over the range's k-blocks, grouped by tile."""
+    lo, hi = streamk_range(c, workers, sk_tiles, k_blocks)
+    by_tile = {}
+    for g in range(lo, hi):
+        by_tile.setdefault(g // k_blocks, []).append(g % k_blocks)
+    segs = []
+    for t, ks in by_tile.items():
+        assert ks == list(range(ks[0], ks[-1] + 1))
+        segs.append((t, ks[0], ks[-1] + 1, ks[-1] == k_blocks - 1))
+    segs.sort(key=lambda s: s[3])            # contributions first, the owned tile last
+    return segs
+
+
+def streamk_contributors(t, workers, sk_tiles, k_blocks):
+    """(owner, [contributing workers]) of tail tile t: every worker whose range meets the tile,
+    the owner being the one holding its last k-block."""
+    meets = []
+    for c in range(workers):
+        lo, hi = streamk_range(c, workers, sk_tiles, k_blocks)
+        if lo < hi and lo < (t + 1) * k_blocks and hi > t * k_blocks:
+            meets.append(c)
+    owner = [c for c in meets
+             if streamk_range(c, workers, sk_tiles, k_blocks)[0] <= (t + 1) * k_blocks - 1
+             < streamk_range(c, workers, sk_tiles, k_blocks)[1]]
+    assert len(owner) == 1
+    return owner[0], [c for c in meets if c != owner[0]]
+
+
+def enumerate_units_streamk(m_blocks, n_blocks, num_workers, group, k_blocks,
+                            column_major=False):
+    """Rows (worker, w, bx, by, part, k_lo, k_hi, unit) of the traversal with the stream-K
+    tail: whole tiles (part -1, k 0..KB, unit = their linear id) on the grid stride, then each
+    worker's tail segments in walking order (part 2 = a contribution, 3 = the owned tile; unit =
+    D + 2c + part - 2, D = the number of whole tiles).  Ordered by worker, then w."""
+    if min(m_blocks, n_blocks, num_workers, group, k_blocks) < 1:
+        raise ValueError("m_blocks, n_blocks, num_workers, group and k_blocks must be >= 1")
+    decode = tile_coord_column_major if column_major else tile_coord
+    total = m_blocks * n_blocks
+    sk = total % num_workers
+    whole = total - sk
+    rows = []
+    for c in range(num_workers):
+        w = 0
+        while c + w * num_workers < whole:
+            bx, by = decode(c + w * num_workers, m_blocks, n_blocks, group)
+            rows.append((c, w, bx, by, -1, 0, k_blocks, c + w * num_workers))
+            w += 1
+        if sk:
+            for (t, k_lo, k_hi, owns) in streamk_segments(c, num_workers, sk, k_blocks):
+                bx, by = decode(whole + t, m_blocks, n_blocks, group)
+                part = 3 if owns else 2
+                rows.append((c, w, bx, by, part, k_lo, k_hi, whole + 2 * c + part - 2))
+                w += 1
+    return rows
