@@ -72,6 +72,12 @@ enum {
   /* tg_gemm_launch_shape flag: describe the block-scaled MXFP8 GEMM's launch (tg_gemm_mxfp8*),
      whose variants are SINGLE and PAIR, instead of the dense GEMM's. */
   TG_SHAPE_MXFP8 = 0x1000,
+  /* OR'ed into a PAIR, PAIR_WIDE or AUTO variant of tg_gemm_persistent_ws or
+     tg_gemm_persistent_debug (with a workspace): split the last partial wave of tiles along K
+     (the stream-K tail described at tg_gemm_persistent_ws) whenever there is one. */
+  TG_SCHEDULE_STREAMK = 0x2000,
+  /* tg_gemm_launch_shape flag: describe the launch of tg_gemm_persistent_ws (with a workspace). */
+  TG_SHAPE_WORKSPACE = 0x4000,
   /* tg_tile_schedule_ex flag: apply the tail split (the GEMM does unless TG_SCHEDULE_PLAIN) */
   TG_SCHEDULE_SPLIT_TAIL = 0x1
 };
@@ -119,6 +125,41 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
  */
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev,
                           int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant);
+
+/*
+ * tg_gemm_persistent_ws -- tg_gemm_persistent_ex with a workspace.  With TG_SCHEDULE_STREAMK
+ * in ``variant`` the CTA-pair variants split the last partial wave of tiles along K (a stream-K
+ * tail) instead of cutting its tiles into half-width units.  With T tiles over P CTA pairs, the
+ * R = T mod P tiles that come last in the traversal have their k-blocks, numbered tile-major,
+ * cut into P contiguous ranges, one per pair.  The pair holding a tail tile's last k-block owns
+ * the tile: the other pairs that meet it write their fp32 partial sums to the workspace, and the
+ * owner adds them to its own before converting and storing the tile.  Each pair works its
+ * contribution before the tile it owns, so an owner waits only on lower-numbered pairs.  The
+ * library never takes this tail unasked (AUTO included): measured on GB300 it was slower than
+ * the half-width units at every size tried, the partial sums' round trip costing about what the
+ * idle part of the last wave does.  Without TG_SCHEDULE_STREAMK the workspace is unused.
+ * Results are those of tg_gemm_persistent_ex up to the order of fp32 additions (bit-identical
+ * where the sums are exact).
+ *   workspace_dev: NULL, or a device buffer of workspace_bytes, 256-byte aligned, of at least
+ *     tg_gemm_workspace_bytes(M, N, K, variant) bytes; its contents need no initialisation and
+ *     are scratch.  It must not be used by another call that may run at the same time (another
+ *     stream).  TG_SCHEDULE_STREAMK with NULL or a smaller buffer: TG_ERR_ARG.
+ *     TG_SCHEDULE_PLAIN and the single-CTA variant never take the stream-K tail.
+ * Every wait on another pair is bounded by the watchdog (TG_ERR_TIMEOUT through
+ * tg_device_status).  Same argument rules and errors as tg_gemm_persistent_ex otherwise.
+ */
+int tg_gemm_persistent_ws(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
+                          int64_t N, int64_t K, int dtype, void* stream, int variant,
+                          void* workspace_dev, int64_t workspace_bytes);
+
+/*
+ * tg_gemm_workspace_bytes -- the workspace tg_gemm_persistent_ws needs for this problem and
+ * variant (TG_SCHEDULE_STREAMK included) on the current device: 0 when it takes no stream-K tail;
+ * otherwise (pairs x 8) flags of 4 bytes padded to 256, then one fp32 slice of 128 x tile_n per
+ * pair and CTA.
+ * Returns the byte count or a negative error code.
+ */
+int64_t tg_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant);
 
 /*
  * tg_tile_schedule -- the tile order the GEMM kernel follows, for inspection.
@@ -196,12 +237,17 @@ int tg_gemm_config(int* block_m, int* block_n, int* block_k, int* stages, int* g
  *   split_from == units: no split); *group, *column_major: the traversal (the grouped order's
  *   width and whether it runs along M first).  With TG_VARIANT_AUTO and no TG_SCHEDULE_PLAIN,
  *   TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP flag, the library also picks the traversal,
- *   as tg_gemm_persistent_ex describes.  Any pointer may be NULL.
+ *   as tg_gemm_persistent_ex describes.  With TG_SHAPE_WORKSPACE: the launch of
+ *   tg_gemm_persistent_ws; *sk_tiles: the stream-K tail's tiles (0: none), which then follow the
+ *   split_from whole tiles, and unit ids run to *units = split_from + 2 x workers (pair c's
+ *   contribution is unit split_from + 2c, its owned tile split_from + 2c + 1);
+ *   *workspace_bytes: the workspace that launch needs.  Any pointer may be NULL.
  * Queries the device once (first call); launches nothing.  Returns TG_OK or an error.
  */
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
-                         int* ctas, int* split_from, int* units, int* group, int* column_major);
+                         int* ctas, int* split_from, int* units, int* group, int* column_major,
+                         int* sk_tiles, int64_t* workspace_bytes);
 
 /*
  * tg_gemm_persistent_debug -- the same GEMM, synchronously, with two inspection aids.
@@ -217,11 +263,14 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
  *     call must return TG_ERR_TIMEOUT with the context intact.  In the CTA-pair kernels CTA 0 is
  *     the even CTA of pair 0 (the other CTA of the pair still fills the phase) and CTA 1 the odd
  *     one (the even CTA has armed the phase for both).
+ *   workspace_dev, workspace_bytes: as in tg_gemm_persistent_ws (NULL, 0: none); a stream-K
+ *     tail segment's trace row has part 2 (a contribution) or 3 (an owned tile).
  * Synchronises ``stream``.  Returns TG_OK, TG_ERR_TIMEOUT or another error.
  */
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev,
                              int64_t M, int64_t N, int64_t K, int dtype, void* stream, int variant,
-                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase);
+                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase,
+                             void* workspace_dev, int64_t workspace_bytes);
 
 /*
  * tg_device_status -- synchronises ``stream``, then reads and clears the current device's

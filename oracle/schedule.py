@@ -116,7 +116,7 @@ def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True, col
 
 # ---------------------------------------------------------------- stream-K tail
 # Reading beyond the pages (their scheduler walks whole tiles): the library can instead split
-# the last partial wave along K.  With T tiles and P workers, the R = T mod P tiles that come
+# the last partial wave along K (on request; it never does by itself).  With T tiles and P workers, the R = T mod P tiles that come
 # last in the traversal form the tail; their k-blocks, numbered tile-major (tile i of the tail
 # owns numbers i*KB .. i*KB + KB - 1), are cut into P contiguous ranges, worker c taking
 # [floor(c*R*KB/P), floor((c+1)*R*KB/P)).  The whole tiles before the tail keep the grid stride.
@@ -125,16 +125,6 @@ def enumerate_units(m_blocks, n_blocks, num_workers, group, split_tail=True, col
 # sums of the tile to its own and stores the tile.  A worker walks its part of the later tile
 # (a contribution) before its part of the earlier one (which it owns), so every owner waits only
 # for lower-numbered workers' contributions, each made first in its worker's range.
-
-
-def streamk_applies(tiles, workers, k_blocks):
-    """The library's rule for taking the stream-K tail when a workspace is given: the partial
-    wave holds between a quarter of a wave (a tail tile then has about four contributors at
-    most) and four fifths of one (above that a whole last wave costs less than a fifth of a
-    tile's time more than the tail's work, about what the partial sums' round trip costs), and
-    every worker gets at least eight k-blocks of it."""
-    rem = tiles % workers
-    return rem > 0 and 4 * rem >= workers and 5 * rem <= 4 * workers and rem * k_blocks >= 8 * workers
 
 
 def streamk_range(c, workers, sk_tiles, k_blocks):

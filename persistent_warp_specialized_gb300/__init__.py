@@ -32,6 +32,8 @@ TG_SCHEDULE_SPLIT_TAIL = 0x1
 TG_SCHEDULE_DYNAMIC = 0x400
 TG_EPILOGUE_DIRECT = 0x800
 TG_SHAPE_MXFP8 = 0x1000
+TG_SCHEDULE_STREAMK = 0x2000
+TG_SHAPE_WORKSPACE = 0x4000
 TG_SCHEDULE_NOALLOC_MAX_UNITS = 65536   # scratch rows of tg_tile_schedule_noalloc
 VARIANTS = {"auto": TG_VARIANT_AUTO, "single": TG_VARIANT_SINGLE, "pair": TG_VARIANT_PAIR,
             "wide": TG_VARIANT_PAIR_WIDE}
@@ -41,6 +43,8 @@ DTYPES = {"f16": TG_F16, "bf16": TG_BF16}
 EXPORTED = (
     "tg_gemm_persistent",
     "tg_gemm_persistent_ex",
+    "tg_gemm_persistent_ws",
+    "tg_gemm_workspace_bytes",
     "tg_tile_schedule",
     "tg_tile_schedule_ex",
     "tg_tile_schedule_noalloc",
@@ -81,6 +85,10 @@ def load_library(path=LIB_PATH):
     lib.tg_gemm_persistent.restype = i32
     lib.tg_gemm_persistent_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32]
     lib.tg_gemm_persistent_ex.restype = i32
+    lib.tg_gemm_persistent_ws.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, i64]
+    lib.tg_gemm_persistent_ws.restype = i32
+    lib.tg_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32]
+    lib.tg_gemm_workspace_bytes.restype = i64
     lib.tg_tile_schedule.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.tg_tile_schedule.restype = i32
     lib.tg_tile_schedule_ex.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
@@ -93,10 +101,11 @@ def load_library(path=LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.tg_gemm_config.argtypes = [ip, ip, ip, ip, ip]
     lib.tg_gemm_config.restype = i32
-    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32] + [ip] * 11
+    lib.tg_gemm_launch_shape.argtypes = [i64, i64, i64, i32] + [ip] * 12 + [
+        ctypes.POINTER(ctypes.c_int64)]
     lib.tg_gemm_launch_shape.restype = i32
     lib.tg_gemm_persistent_debug.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, vp, u64,
-                                             i64]
+                                             i64, vp, i64]
     lib.tg_gemm_persistent_debug.restype = i32
     lib.tg_device_status.argtypes = [vp]
     lib.tg_device_status.restype = i32
@@ -168,13 +177,25 @@ def _group(g):
     return int(g) << 16
 
 
-def _variant(v, plain=False, column_major=False, dynamic=False, group=None, direct=False):
+def _variant(v, plain=False, column_major=False, dynamic=False, group=None, direct=False,
+             streamk=False):
     """"auto" / "single" / "pair" / "wide" (or a TG_VARIANT_* int) plus the schedule flags."""
     code = VARIANTS[v] if isinstance(v, str) else int(v)
     return (code | (TG_SCHEDULE_PLAIN if plain else 0)
             | (TG_SCHEDULE_COLUMN_MAJOR if column_major else 0)
             | (TG_SCHEDULE_DYNAMIC if dynamic else 0) | _group(group)
-            | (TG_EPILOGUE_DIRECT if direct else 0))
+            | (TG_EPILOGUE_DIRECT if direct else 0)
+            | (TG_SCHEDULE_STREAMK if streamk else 0))
+
+
+def _nbytes(ws, workspace_bytes):
+    if ws is None:
+        return 0
+    if workspace_bytes is not None:
+        return int(workspace_bytes)
+    if hasattr(ws, "numel") and hasattr(ws, "element_size"):
+        return ws.numel() * ws.element_size()
+    raise ValueError("workspace_bytes is needed for a raw workspace pointer")
 
 
 def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", plain=False,
@@ -187,13 +208,34 @@ def tg_gemm_persistent_ex(A, B, C, M, N, K, dtype, stream=None, variant="auto", 
         _variant(variant, plain, column_major, dynamic, group, direct)))
 
 
+def tg_gemm_persistent_ws(A, B, C, M, N, K, dtype, workspace, stream=None, variant="auto",
+                          plain=False, column_major=False, group=None, streamk=False,
+                          workspace_bytes=None):
+    """tg_gemm_persistent_ex with a workspace (a CUDA tensor of at least tg_gemm_workspace_bytes
+    bytes, or None); with ``streamk`` the CTA-pair kernels split the last partial wave of tiles
+    along K (the stream-K tail) whenever there is one."""
+    return _check(load_library().tg_gemm_persistent_ws(
+        _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
+        _variant(variant, plain, column_major, False, group, False, streamk), _ptr(workspace),
+        _nbytes(workspace, workspace_bytes)))
+
+
+def tg_gemm_workspace_bytes(M, N, K, variant="auto", plain=False, column_major=False,
+                            group=None, streamk=False):
+    """Workspace bytes tg_gemm_persistent_ws needs on the current device (0: none)."""
+    n = load_library().tg_gemm_workspace_bytes(
+        M, N, K, _variant(variant, plain, column_major, False, group, False, streamk))
+    return _check(n) if n < 0 else n
+
+
 def tg_gemm_persistent_debug(A, B, C, M, N, K, dtype, stream=None, variant="auto", trace=None,
                              watchdog_ns=0, inject_skip_phase=-1, plain=False,
-                             column_major=False, dynamic=False, group=None):
+                             column_major=False, dynamic=False, group=None, workspace=None,
+                             streamk=False, workspace_bytes=None):
     return _check(load_library().tg_gemm_persistent_debug(
         _ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype(dtype), _stream(stream),
-        _variant(variant, plain, column_major, dynamic, group), _ptr(trace), watchdog_ns,
-        inject_skip_phase))
+        _variant(variant, plain, column_major, dynamic, group, False, streamk), _ptr(trace),
+        watchdog_ns, inject_skip_phase, _ptr(workspace), _nbytes(workspace, workspace_bytes)))
 
 
 def tg_gemm_persistent_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, M, N, K, dtype,
@@ -215,15 +257,22 @@ def tg_gemm_config():
 
 
 def tg_gemm_launch_shape(M, N, K, variant="auto", plain=False, dynamic=False,
-                         column_major=False, group=None, mxfp8=False):
+                         column_major=False, group=None, mxfp8=False, workspace=False,
+                         streamk=False):
     """The persistent launch (and traversal) the library uses for M x N x K on the current
-    device: of the dense GEMM, or with ``mxfp8`` of the block-scaled MXFP8 GEMM."""
-    vals = [ctypes.c_int() for _ in range(11)]
-    code = _variant(variant, plain, column_major, dynamic, group) | (TG_SHAPE_MXFP8 if mxfp8 else 0)
-    _check(load_library().tg_gemm_launch_shape(M, N, K, code, *[ctypes.byref(v) for v in vals]))
+    device: of the dense GEMM, or with ``mxfp8`` of the block-scaled MXFP8 GEMM; with
+    ``workspace`` the launch of tg_gemm_persistent_ws (with ``streamk``: the stream-K tail)."""
+    vals = [ctypes.c_int() for _ in range(12)]
+    ws = ctypes.c_int64()
+    code = (_variant(variant, plain, column_major, dynamic, group, False, streamk)
+            | (TG_SHAPE_MXFP8 if mxfp8 else 0) | (TG_SHAPE_WORKSPACE if workspace else 0))
+    _check(load_library().tg_gemm_launch_shape(M, N, K, code, *[ctypes.byref(v) for v in vals],
+                                               ctypes.byref(ws)))
     keys = ("variant", "tile_m", "tile_n", "m_tiles", "n_tiles", "workers", "ctas",
-            "split_from", "units", "group", "column_major")
-    return dict(zip(keys, (v.value for v in vals)))
+            "split_from", "units", "group", "column_major", "sk_tiles")
+    out = dict(zip(keys, (v.value for v in vals)))
+    out["workspace_bytes"] = ws.value
+    return out
 
 
 def tg_tile_schedule(m_blocks, n_blocks, num_sms, group):

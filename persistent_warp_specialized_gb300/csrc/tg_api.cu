@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -241,15 +242,36 @@ Raster auto_raster(int64_t M, int64_t N, int64_t K, uint32_t m_tiles, uint32_t n
   return {static_cast<uint32_t>(tg::kGroup), 0u};
 }
 
+// Workspace of the stream-K tail: one flag per (worker, CTA, epilogue warp), padded to 256
+// bytes, then one fp32 slice of 128 rows x tile_n per (worker, CTA).
+uint64_t sk_flag_bytes(uint32_t workers) {
+  return (uint64_t(workers) * 2 * tg::kEpiWarps * 4 + 255) / 256 * 256;
+}
+uint64_t sk_partial_bytes(uint32_t workers, uint32_t tile_n) {
+  return uint64_t(workers) * 2 * tg::kBM * tile_n * 4;
+}
+
 struct Shape {
   uint32_t tile_m, tile_n, m_tiles, n_tiles, workers, ctas, split_from, units;
+  uint32_t sk_tiles;       // stream-K tail tiles (0: none); then units = split_from = whole tiles
+  uint64_t sk_bytes;       // workspace the stream-K tail needs
 };
+
+int block_k_of(int variant) {
+  return variant == TG_VARIANT_PAIR        ? tg::kPairBK
+         : variant == TG_VARIANT_PAIR_WIDE ? tg::kWideBK
+                                           : tg::kBK;
+}
 
 // Persistent launch of a concrete variant: one worker per SM (SINGLE) or per resident CTA
 // pair (PAIR), never more workers than work units; the last partial wave is split into
-// half-width units unless ``plain`` (the page's traversal) is asked for.
-Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain, bool dynamic,
-                   int sms, int max_pairs) {
+// half-width units unless ``plain`` (the page's traversal) is asked for, or, for the CTA-pair
+// variants when ``streamk`` is asked for (with a workspace), along K (the stream-K tail of
+// tg_tile_scheduler.cuh).  The library never takes the stream-K tail by itself: measured on
+// GB300 it lost to the half-width units at every size tried (the partial sums' round trip
+// through memory costs about what the idle part of the last wave does).
+Shape launch_shape(int64_t M, int64_t N, int64_t K, int variant, bool plain, bool dynamic,
+                   int sms, int max_pairs, bool streamk = false) {
   Shape sh;
   sh.tile_m = pair_variant(variant) ? tg::kPairBM : tg::kBM;
   sh.tile_n = variant == TG_VARIANT_PAIR_WIDE ? tg::kWideBN : tg::kBN;
@@ -257,6 +279,19 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
   sh.n_tiles = static_cast<uint32_t>((N + sh.tile_n - 1) / sh.tile_n);
   const uint32_t tiles = sh.m_tiles * sh.n_tiles;
   const uint32_t slots = pair_variant(variant) ? uint32_t(max_pairs) : uint32_t(sms);
+  const uint32_t bk = static_cast<uint32_t>(block_k_of(variant));
+  const uint32_t k_blocks = static_cast<uint32_t>((uint64_t(K) + bk - 1) / bk);
+  sh.sk_tiles = 0;
+  sh.sk_bytes = 0;
+  const uint32_t rem = tiles % slots;
+  if (streamk && !plain && !dynamic && pair_variant(variant) && k_blocks > 0 && rem > 0) {
+    sh.sk_tiles = rem;
+    sh.split_from = sh.units = tiles - rem;
+    sh.workers = slots;   // every worker takes a range of the tail
+    sh.ctas = 2 * sh.workers;
+    sh.sk_bytes = sk_flag_bytes(sh.workers) + sk_partial_bytes(sh.workers, sh.tile_n);
+    return sh;
+  }
   if (plain) {
     sh.split_from = sh.units = tiles;
   } else {
@@ -271,7 +306,8 @@ Shape launch_shape(int64_t M, int64_t N, int64_t /*K*/, int variant, bool plain,
 
 constexpr int kGroupBits = TG_SCHEDULE_GROUP(0xFF);
 constexpr int kScheduleFlags = TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR |
-                               TG_SCHEDULE_DYNAMIC | TG_EPILOGUE_DIRECT | kGroupBits;
+                               TG_SCHEDULE_DYNAMIC | TG_EPILOGUE_DIRECT | TG_SCHEDULE_STREAMK |
+                               kGroupBits;
 
 bool known_variant(int v) {
   const int kernel = v & ~kScheduleFlags;
@@ -292,10 +328,28 @@ bool auto_traversal(int variant) {
          (variant & (TG_SCHEDULE_PLAIN | TG_SCHEDULE_COLUMN_MAJOR | kGroupBits)) == 0;
 }
 
+// Epoch of a launch with a stream-K tail: never 0, distinct for 2^32 - 1 launches.
+std::atomic<uint32_t> g_sk_epoch{0};
+
+uint32_t next_sk_epoch() {
+  uint32_t e = ++g_sk_epoch;
+  while (e == 0) e = ++g_sk_epoch;
+  return e;
+}
+
 int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
               void* stream, int variant, bool debug, int32_t* trace, uint64_t watchdog_ns,
-              int64_t inject) {
+              int64_t inject, void* workspace = nullptr, int64_t workspace_bytes = 0) {
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  const bool force_sk = (variant & TG_SCHEDULE_STREAMK) != 0;
+  if (force_sk && !workspace) return fail(TG_ERR_ARG, "TG_SCHEDULE_STREAMK needs a workspace");
+  if (workspace_bytes < 0) return fail(TG_ERR_ARG, "negative workspace size");
+  if (workspace) {
+    int rc = check_device_ptr(workspace, "workspace");
+    if (rc != TG_OK) return rc;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(TG_ERR_ALIGN, "the workspace must be 256-byte aligned");
+  }
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   uint32_t column_major = (variant & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
@@ -320,16 +374,18 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   }
   tg::GemmLaunch l;
   if ((rc = encode_2d(&l.tmA, dtype, A, K, M, tg::kKAtom, tg::kBM, "A")) != TG_OK) return rc;
-  const int block_k = variant == TG_VARIANT_PAIR        ? tg::kPairBK
-                      : variant == TG_VARIANT_PAIR_WIDE ? tg::kWideBK
-                                                        : tg::kBK;
+  const int block_k = block_k_of(variant);
   if ((rc = encode_2d(&l.tmB, dtype, B, N, K, tg::kBChunkCols, block_k, "B")) != TG_OK) return rc;
   if ((rc = encode_2d(&l.tmC, dtype, C, N, M, tg::kEpiN, 32, "C")) != TG_OK) return rc;
   l.C = C;
   l.M = static_cast<uint32_t>(M);
   l.N = static_cast<uint32_t>(N);
   l.K = static_cast<uint32_t>(K);
-  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs, force_sk);
+  if (sh.sk_tiles && uint64_t(workspace_bytes) < sh.sk_bytes)
+    return fail(TG_ERR_ARG, "workspace of %lld bytes; the stream-K tail needs %llu",
+                static_cast<long long>(workspace_bytes),
+                static_cast<unsigned long long>(sh.sk_bytes));
   if (choose_traversal) {
     const Raster r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles, sh.tile_m, sh.tile_n,
                                  sh.workers);
@@ -349,6 +405,13 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
   l.trace = trace;
   l.inject_skip_phase = inject;
+  l.sk_tiles = sh.sk_tiles;
+  l.sk_epoch = sh.sk_tiles ? next_sk_epoch() : 0u;
+  l.sk_slot_f4 = tg::kBM * sh.tile_n / 4;
+  l.sk_flags = sh.sk_tiles ? static_cast<uint32_t*>(workspace) : nullptr;
+  l.sk_partials = sh.sk_tiles ? reinterpret_cast<float4*>(static_cast<char*>(workspace) +
+                                                          sk_flag_bytes(sh.workers))
+                              : nullptr;
   cudaError_t e;
   if (debug && (e = tg::clear_watchdog_status(s)) != cudaSuccess)
     return fail_cuda("clearing the watchdog word", e);
@@ -577,16 +640,38 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev, int64_
 
 int tg_gemm_persistent_ex(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
                           int64_t N, int64_t K, int dtype, void* stream, int variant) {
+  if (variant & TG_SCHEDULE_STREAMK)
+    return fail(TG_ERR_ARG, "TG_SCHEDULE_STREAMK needs a workspace (tg_gemm_persistent_ws)");
   return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, false, nullptr, 0, -1);
+}
+
+int tg_gemm_persistent_ws(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
+                          int64_t N, int64_t K, int dtype, void* stream, int variant,
+                          void* workspace_dev, int64_t workspace_bytes) {
+  return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, false, nullptr, 0, -1,
+                   workspace_dev, workspace_bytes);
+}
+
+int64_t tg_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant) {
+  int sk_tiles = 0;
+  int64_t bytes = 0;
+  int rc = tg_gemm_launch_shape(M, N, K, variant | TG_SHAPE_WORKSPACE, nullptr, nullptr, nullptr,
+                                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                nullptr, &sk_tiles, &bytes);
+  return rc != TG_OK ? rc : bytes;
 }
 
 int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* variant_out,
                          int* tile_m, int* tile_n, int* m_tiles, int* n_tiles, int* workers,
                          int* ctas, int* split_from, int* units, int* group,
-                         int* column_major) {
+                         int* column_major, int* sk_tiles, int64_t* workspace_bytes) {
   const bool mxfp8 = (variant & TG_SHAPE_MXFP8) != 0;
-  variant &= ~TG_SHAPE_MXFP8;
+  const bool with_ws = (variant & TG_SHAPE_WORKSPACE) != 0;
+  variant &= ~(TG_SHAPE_MXFP8 | TG_SHAPE_WORKSPACE);
   if (!known_variant(variant)) return fail(TG_ERR_ARG, "unknown variant %d", variant);
+  const bool force_sk = (variant & TG_SCHEDULE_STREAMK) != 0;
+  if (force_sk && (mxfp8 || !with_ws))
+    return fail(TG_ERR_ARG, "TG_SCHEDULE_STREAMK: dense GEMM with a workspace only");
   const bool plain = (variant & TG_SCHEDULE_PLAIN) != 0;
   const bool dynamic = (variant & TG_SCHEDULE_DYNAMIC) != 0;
   const bool choose_traversal = auto_traversal(variant) && !mxfp8;
@@ -603,7 +688,8 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
     variant = mxfp8 ? auto_variant(M, N, K, max_pairs) : auto_variant_dense(M, N, K, max_pairs);
   if (dynamic && variant != TG_VARIANT_SINGLE)
     return fail(TG_ERR_ARG, "TG_SCHEDULE_DYNAMIC needs the single-CTA variant");
-  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs);
+  const Shape sh = launch_shape(M, N, K, variant, plain, dynamic, sms, max_pairs,
+                                with_ws && !mxfp8 && force_sk);
   if (choose_traversal)
     r = auto_raster(M, N, K, sh.m_tiles, sh.n_tiles, sh.tile_m, sh.tile_n, sh.workers);
   if (variant_out) *variant_out = variant;
@@ -616,19 +702,23 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
   if (workers) *workers = static_cast<int>(sh.workers);
   if (ctas) *ctas = static_cast<int>(sh.ctas);
   if (split_from) *split_from = static_cast<int>(sh.split_from);
-  if (units) *units = static_cast<int>(sh.units);
+  // with a stream-K tail, unit ids (the debug trace's rows) run up to split_from + 2 workers
+  if (units) *units = static_cast<int>(sh.sk_tiles ? sh.units + 2 * sh.workers : sh.units);
+  if (sk_tiles) *sk_tiles = static_cast<int>(sh.sk_tiles);
+  if (workspace_bytes) *workspace_bytes = static_cast<int64_t>(sh.sk_bytes);
   return TG_OK;
 }
 
 int tg_gemm_persistent_debug(const void* A_dev, const void* B_dev, void* C_dev, int64_t M,
                              int64_t N, int64_t K, int dtype, void* stream, int variant,
-                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase) {
+                             int32_t* trace_dev, uint64_t watchdog_ns, int64_t inject_skip_phase,
+                             void* workspace_dev, int64_t workspace_bytes) {
   if (trace_dev) {
     int rc = check_device_ptr(trace_dev, "trace");
     if (rc != TG_OK) return rc;
   }
   return gemm_impl(A_dev, B_dev, C_dev, M, N, K, dtype, stream, variant, true, trace_dev,
-                   watchdog_ns, inject_skip_phase);
+                   watchdog_ns, inject_skip_phase, workspace_dev, workspace_bytes);
 }
 
 // Runs the device scheduler over [0, units) and copies rows of ``width`` int32 (4: without

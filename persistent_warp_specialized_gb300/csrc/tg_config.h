@@ -113,6 +113,8 @@ constexpr uint32_t kPairSmemBytes = kSmemAlignSlack + kPairStages * kPairStageBy
 static_assert(kPairSmemBytes + 256 <= 232448, "shared memory per CTA (pair variant)");
 static_assert(kPairBNHalf % kBChunkCols == 0, "pair B half must be whole 64-column chunks");
 static_assert(kPairBK % kKAtom == 0 && kPairBK <= 256, "pair block_K: a multiple of 64, <= 256");
+static_assert(kPairStages * kPairStageBytes / kEpiWarps >= (kBN / kEpiN) * 8192,
+              "a stream-K owner stages one contribution per epilogue warp in the operand ring");
 
 // Block-scaled MXFP8 kernel (the PR's gemm_mxfp8_blockscaled_1d1d): E4M3 A [M, K] and B [N, K],
 // both K-major, one E8M0 scale per 32 K-elements of each A row and each B column, fp32

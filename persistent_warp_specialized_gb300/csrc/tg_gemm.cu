@@ -68,6 +68,11 @@ GemmParams params_of(const GemmLaunch& l) {
   p.watchdog_ns = l.watchdog_ns;
   p.trace = l.trace;
   p.inject_skip_phase = l.inject_skip_phase;
+  p.sk_tiles = l.sk_tiles;
+  p.sk_epoch = l.sk_epoch;
+  p.sk_slot_f4 = l.sk_slot_f4;
+  p.sk_flags = l.sk_flags;
+  p.sk_partials = l.sk_partials;
   return p;
 }
 

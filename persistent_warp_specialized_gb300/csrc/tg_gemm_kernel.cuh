@@ -58,6 +58,12 @@ struct GemmParams {
   uint64_t watchdog_ns;
   int32_t* trace;              // debug instantiation only; may be null (5 int32 per unit)
   int64_t inject_skip_phase;   // debug instantiation only; -1 = none
+  // stream-K tail of the CTA-pair kernels (tg_streamk.cuh); sk_tiles = 0: none
+  uint32_t sk_tiles;
+  uint32_t sk_epoch;           // this launch's flag value
+  uint32_t sk_slot_f4;         // float4s per (worker, CTA) partial slot
+  uint32_t* sk_flags;
+  float4* sk_partials;
 };
 
 // Debug fault injection: ``inject`` = cta * 2^32 + phase names a pipeline phase that the producer
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
-        const bool half = sched.part >= 0;              // half-width unit of the tail split
+        const bool half = sched.half_unit();              // half-width unit of the tail split
         const int32_t m0 = static_cast<int32_t>(sched.m_idx) * kBM;
         const int32_t n0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
         const uint32_t b_chunks = half ? kBN / kBChunkCols / 2 : kBN / kBChunkCols;
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBN;
-        const uint32_t idesc = sched.part >= 0 ? idesc_half : idesc_full;
+        const uint32_t idesc = sched.half_unit() ? idesc_half : idesc_full;
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
           const uint32_t s = static_cast<uint32_t>(phase % kStages);
@@ -464,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
-      const bool half = sched.part >= 0;
+      const bool half = sched.half_unit();
       const int32_t row0 = static_cast<int32_t>(sched.m_idx) * kBM + static_cast<int32_t>(q) * 32;
       const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
       const uint32_t chunks = half ? kBN / kEpiN / 2 : kBN / kEpiN;

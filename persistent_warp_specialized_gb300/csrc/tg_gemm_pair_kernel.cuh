@@ -20,6 +20,10 @@
 // CTA's slot at the same offset, and writes 128 rows into each CTA's TMEM.  tcgen05.commit
 // with a CTA mask of 0b11 completes ``consumed[s]`` and ``tmem_full[w & 1]`` in both CTAs.
 // Both CTAs' epilogue warps report on the even CTA's ``tmem_empty[w & 1]`` (pair_report_warp).
+// A unit covers k-blocks sched.k_lo .. k_hi - 1 (all of them except in the stream-K tail), and
+// the ring position is the count of k-blocks the role has handled so far.  In the tail a
+// contribution's accumulator goes to the workspace instead of C, and an owned tile adds the
+// contributions before it is stored (tg_streamk.cuh).
 //
 // All tcgen05 instructions of this kernel use cta_group::2.  Waits are bounded exactly as in
 // the single-CTA kernel; an abort also raises the peer CTA's flag, and the pair meets at a
@@ -29,6 +33,7 @@
 #pragma once
 
 #include "tg_gemm_kernel.cuh"
+#include "tg_streamk.cuh"
 
 namespace tg {
 
@@ -51,6 +56,7 @@ struct __align__(8) PairCtl {
   uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
   PairFills<kPairStages> fills;
   uint32_t sink[kEpiWarps];          // even CTA: target of the odd epilogue warps' st.async
+  uint64_t sk_bar[kEpiWarps];        // per epilogue warp: stream-K contributions landed
   uint32_t tmem_base;
   int abort;
 };
@@ -102,6 +108,115 @@ __device__ __forceinline__ void pair_report_warp(uint32_t bar, uint32_t rank, ui
     else
       st_async_u32(sink_even, 0u, mapa_shared(bar, 0));
   }
+}
+
+// Waits (every lane, acquire at gpu scope) until a stream-K flag holds ``epoch``; bounded like
+// pair_wait_or_abort.  The contributor is a lower-numbered worker that started its tail before
+// this one, so the wait ends unless a peer stopped.
+__device__ __forceinline__ bool sk_wait_flag(const uint32_t* flag, uint32_t epoch,
+                                             volatile int* abort_flag, uint32_t peer_abort_addr,
+                                             uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag) == epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ld_acquire_gpu(flag) == epoch) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      st_shared_cluster_u32(peer_abort_addr, 1u);
+      atomicOr(&g_watchdog_status, kRoleEpilogue);
+      return false;
+    }
+  }
+}
+
+// Contribution of one epilogue warp: its lanes' fp32 accumulator, ``chunks`` chunks of 64
+// columns from TMEM address t_col (chunk indices c0 ..), staged through the warp's two 4 KiB
+// buffers (half a chunk each) and bulk-stored into ``slot``.  Lane 0 issues the copies; the
+// caller publishes (sk_publish), which waits for them.
+__device__ __forceinline__ void sk_write_slot(float4* slot, uint32_t t_col, uint32_t chunks,
+                                              uint32_t c0, uint32_t q, uint32_t lane,
+                                              uint32_t sbuf0, uint32_t sbuf1) {
+  if (lane == 0) bulk_wait_group_read<0>();   // earlier stores are done reading the buffers
+  __syncwarp();
+#pragma unroll 1
+  for (uint32_t j = 0; j < chunks; ++j) {
+    uint32_t v[64];
+    tmem_ld_32x32b_x64(t_col + j * kEpiN, v);
+#pragma unroll
+    for (uint32_t hh = 0; hh < 2; ++hh) {
+      const uint32_t buf = hh ? sbuf1 : sbuf0;
+      if (j > 0 || hh > 0) {
+        if (lane == 0) bulk_wait_group_read<1>();   // the other buffer's copy may still read
+        __syncwarp();
+      }
+#pragma unroll
+      for (uint32_t g = 0; g < 8; ++g)
+        st_shared_v4(buf + (g * 32u + lane) * 16u, v[4 * (8 * hh + g)], v[4 * (8 * hh + g) + 1],
+                     v[4 * (8 * hh + g) + 2], v[4 * (8 * hh + g) + 3]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_store(slot + sk_chunk_f4(c0 + j, q) + 8u * hh * 32u, buf, 4096u);
+        bulk_commit_group();
+      }
+    }
+  }
+}
+
+// Owner of a stream-K tile, one epilogue warp: adds the contributions of workers c_lo .. c_hi - 1
+// (those with a tail range) to its lanes' fp32 accumulator, ``chunks`` chunks of 64 columns at
+// TMEM address t_col (chunk indices c0 ..): per contribution, wait for its flag (``wait_flags``),
+// bulk-load the warp's part into ``region`` (chunks x 8 KiB of idle shared memory) on the warp's
+// barrier ``bar`` (phase count ``*bar_uses``), then read, add and write back each chunk.  False
+// if a wait ran out or the CTA is stopping.
+__device__ bool sk_gather(const GemmParams& p, uint32_t c_lo, uint32_t c_hi, uint32_t workers,
+                          uint32_t rank, uint32_t q, uint32_t lane, uint32_t t_col,
+                          uint32_t chunks, uint32_t c0, uint32_t region, uint32_t bar,
+                          uint32_t* bar_uses, bool wait_flags, volatile int* abort_flag,
+                          uint32_t peer_abort, uint64_t limit) {
+#pragma unroll 1
+  for (uint32_t c = c_lo; c < c_hi; ++c) {
+    if (!sk_has_range(c, workers, p.sk_tiles, p.k_blocks)) continue;
+    const bool seen = !wait_flags || sk_wait_flag(p.sk_flags + sk_flag_index(c, rank, q),
+                                                  p.sk_epoch, abort_flag, peer_abort, limit);
+    if (!__all_sync(0xffffffffu, seen)) return false;
+    const float4* slot = sk_slot(p.sk_partials, p.sk_slot_f4, c, rank);
+    if (lane == 0) {
+      fence_proxy_async_global();   // the flag was acquired; the copies read after it
+      mbar_arrive_expect_tx(bar, chunks * 8192u);
+      for (uint32_t j = 0; j < chunks; ++j)
+        bulk_load(region + j * 8192u, slot + sk_chunk_f4(c0 + j, q), 8192u, bar);
+    }
+    const bool landed = pair_wait_or_abort(bar, *bar_uses & 1u, abort_flag, peer_abort, limit,
+                                           kRoleEpilogue);
+    ++*bar_uses;
+    if (!__all_sync(0xffffffffu, landed)) return false;
+#pragma unroll 1
+    for (uint32_t j = 0; j < chunks; ++j) {
+      uint32_t v[64];
+      tmem_ld_32x32b_x64(t_col + j * kEpiN, v);
+#pragma unroll
+      for (uint32_t g = 0; g < 16; ++g) {
+        uint32_t x0, x1, x2, x3;
+        ld_shared_v4(region + j * 8192u + (g * 32u + lane) * 16u, x0, x1, x2, x3);
+        v[4 * g] = __float_as_uint(__uint_as_float(v[4 * g]) + __uint_as_float(x0));
+        v[4 * g + 1] = __float_as_uint(__uint_as_float(v[4 * g + 1]) + __uint_as_float(x1));
+        v[4 * g + 2] = __float_as_uint(__uint_as_float(v[4 * g + 2]) + __uint_as_float(x2));
+        v[4 * g + 3] = __float_as_uint(__uint_as_float(v[4 * g + 3]) + __uint_as_float(x3));
+      }
+#pragma unroll
+      for (uint32_t i = 0; i < 4; ++i) {
+        uint32_t (&part)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16 * i]);
+        tmem_st_32x32b_x16(t_col + j * kEpiN + 16u * i, part);
+      }
+      tcgen05_wait_st();
+    }
+    __syncwarp();   // every lane has read the region before the next contribution overwrites it
+  }
+  return true;
 }
 
 template <int S>
@@ -192,6 +307,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_drain, 1);
     mbar_init(smem_u32(&ctl.odd_done), 1);
 #pragma unroll
+    for (int q = 0; q < kEpiWarps; ++q) mbar_init(smem_u32(&ctl.sk_bar[q]), 1);
+#pragma unroll
     for (int st = 0; st < kPairStages; ++st) ctl.fills.par[st] = 0;
     ctl.abort = 0;
     fence_mbarrier_init();
@@ -219,20 +336,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl.abort;
   const uint32_t peer_abort = mapa_shared(smem_u32(&ctl.abort), rank ^ 1u);
   const uint64_t limit = p.watchdog_ns;
-  const uint64_t k_blocks = p.k_blocks;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units, p.column_major);
+                                    p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
       sched.init(pair);
       const uint64_t pol_a = l2_policy<kAPolicy>();
       const uint64_t pol_b = l2_policy<kBPolicy>();
       bool ok = true;
+      uint64_t phase = 0;   // k-blocks filled so far: the ring position of the next one
       while (ok && sched.valid()) {
-        const uint64_t w = sched.current_iter;
-        const bool half = sched.part >= 0;          // half-width unit of the tail split
+        const bool half = sched.half_unit();          // half-width unit of the tail split
         const int32_t m0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM);
         // whole unit: CTA r loads columns [128 r, 128 r + 128) of the 256-wide tile;
         // half unit (128 wide, starting at 128 * part): CTA r loads [64 r, 64 r + 64) of it
@@ -241,8 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  : static_cast<int32_t>(rank) * kPairBNHalf);
         const uint32_t b_chunks = half ? kPairBNHalf / kBChunkCols / 2 : kPairBNHalf / kBChunkCols;
         const uint32_t tx_bytes = 2u * (kPairABytes + b_chunks * kPairBChunkBytes);
-        for (uint32_t k = 0; k < p.k_blocks; ++k) {
-          const uint64_t phase = w * k_blocks + k;
+        for (uint32_t k = sched.k_lo; k < sched.k_hi; ++k, ++phase) {
           const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
           const uint32_t par = static_cast<uint32_t>((phase / kPairStages) & 1u);
           if (!pair_wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, peer_abort, limit,
@@ -288,9 +403,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_full = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
       constexpr uint32_t idesc_half = idesc_f16(DT, kPairBM, kBN / 2, 0, 1);
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units, p.column_major);
+                                    p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
       sched.init(pair);
       bool ok = true;
+      uint64_t phase = 0;
       while (ok && sched.valid()) {
         const uint32_t w = sched.current_iter;
         const uint32_t buf = w & 1u;
@@ -301,9 +417,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * kBN;
-        const uint32_t idesc = sched.part >= 0 ? idesc_half : idesc_full;
-        for (uint32_t k = 0; k < p.k_blocks; ++k) {
-          const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
+        const uint32_t idesc = sched.half_unit() ? idesc_half : idesc_full;
+        for (uint32_t k = sched.k_lo; k < sched.k_hi; ++k, ++phase) {
           const uint32_t s = static_cast<uint32_t>(phase % kPairStages);
           const uint32_t par = static_cast<uint32_t>((phase / kPairStages) & 1u);
           if (!pair_wait_or_abort(bar_loaded + 8u * s, par, abort_flag, peer_abort, limit,
@@ -320,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                    (kk % (kKAtom / kUmmaK)) * kUmmaK * kElemBytes;
             const uint64_t a_desc = smem_desc_sw128(a_addr + a_off, 16, 1024);
             const uint64_t b_desc = smem_desc_sw128(b_addr + kk * kUmmaK * 128u, kPairBChunkBytes, 1024);
-            umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (k | kk) != 0u ? 1u : 0u);
+            umma_f16_pair(d_tmem, a_desc, b_desc, idesc, (k != sched.k_lo || kk != 0u) ? 1u : 0u);
           }
           umma_commit_pair_multicast(bar_consumed + 8u * s, 0x3);
         }
@@ -337,9 +452,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t q = warp - kFirstEpiWarp;
     const uint32_t sink_even = mapa_shared(smem_u32(&ctl.sink[q]), 0);
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units, p.column_major);
+                                    p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
     sched.init(pair);
     uint32_t chunk = 0;
+    uint32_t sk_bar_uses = 0;   // phases of ctl.sk_bar[q] used so far
     while (sched.valid()) {
       const uint32_t w = sched.current_iter;
       const uint32_t buf = w & 1u;
@@ -347,23 +463,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           peer_abort, limit, kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
-      const bool half = sched.part >= 0;
+      const bool half = sched.half_unit();
       const int32_t row0 =
           static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM + q * 32u);
       const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kBN + (half ? sched.part * (kBN / 2) : 0);
       const uint32_t chunks = half ? kBN / kEpiN / 2 : kBN / kEpiN;
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kBN;
+      // stream-K tail: a contribution goes to this worker's slot (no store); an owned tile first
+      // adds the contributions of workers sk_lowest_worker .. pair - 1 into its accumulator
+      const int32_t kind = sched.part;
+      if (kind == 2) {
+        sk_write_slot(sk_slot(p.sk_partials, p.sk_slot_f4, pair, rank), t_row, chunks, 0, q,
+                      lane, sEpi + q * 2u * kEpiBufBytes, sEpi + (q * 2u + 1u) * kEpiBufBytes);
+        tcgen05_fence_before_sync();
+        pair_report_warp(bar_tmem_empty + 8u * buf, rank, lane, sink_even);
+        sk_publish(p.sk_flags + sk_flag_index(pair, rank, q), p.sk_epoch, lane);
+      } else {
+        if (kind == 3 &&
+            !sk_gather(p, sk_lowest_worker(pair, num_pairs, p.sk_tiles, p.k_blocks, sched.sk_tile),
+                       pair, num_pairs, rank, q, lane, t_row, chunks, 0,
+                       sA0 + q * (kPairStages * kPairStageBytes / kEpiWarps),
+                       smem_u32(&ctl.sk_bar[q]), &sk_bar_uses, true, abort_flag, peer_abort,
+                       limit))
+          break;
 #pragma unroll 1
-      for (uint32_t j = 0; j < chunks; ++j, ++chunk) {
-        uint32_t v[64];
-        tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
-        if (j == chunks - 1) {
-          tcgen05_fence_before_sync();
-          pair_report_warp(bar_tmem_empty + 8u * buf, rank, lane, sink_even);
+        for (uint32_t j = 0; j < chunks; ++j, ++chunk) {
+          uint32_t v[64];
+          tmem_ld_32x32b_x64(t_row + j * kEpiN, v);
+          if (j == chunks - 1) {
+            tcgen05_fence_before_sync();
+            pair_report_warp(bar_tmem_empty + 8u * buf, rank, lane, sink_even);
+          }
+          const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
+          epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
+                                   col0 + static_cast<int32_t>(j * kEpiN));
         }
-        const uint32_t sbuf = sEpi + (q * 2u + (chunk & 1u)) * kEpiBufBytes;
-        epilogue_store_chunk<DT>(v, lane, sbuf, &tmC, p, row0,
-                                 col0 + static_cast<int32_t>(j * kEpiN));
       }
       if (DEBUG && p.trace != nullptr && rank == 0 && q == 0 && lane == 0) {
         int32_t* tr = p.trace + 5ull * sched.linear_idx;

@@ -26,6 +26,7 @@
 #pragma once
 
 #include "tg_gemm_pair_kernel.cuh"
+#include "tg_streamk.cuh"
 #include "tg_wide_config.h"
 
 namespace tg {
@@ -39,6 +40,7 @@ struct __align__(8) WideCtl {
   uint64_t odd_done;                 // even CTA: the odd producer has stopped filling
   PairFills<kWideStages> fills;
   uint32_t sink[kEpiWarps];          // even CTA: target of the odd epilogue warps' st.async
+  uint64_t sk_bar[kEpiWarps];        // per epilogue warp: stream-K contributions landed
   uint32_t tmem_base;
   int abort;
 };
@@ -76,6 +78,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_tmem_full, 1);
     mbar_init(bar_tmem_empty, kEpiWarps);
+#pragma unroll
+    for (int q = 0; q < kEpiWarps; ++q) mbar_init(smem_u32(&ctl.sk_bar[q]), 1);
     mbar_init(bar_tmem_empty + 8u, kEpiWarps);
     mbar_init(bar_drain, 1);
     mbar_init(smem_u32(&ctl.odd_done), 1);
@@ -107,24 +111,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl.abort;
   const uint32_t peer_abort = mapa_shared(smem_u32(&ctl.abort), rank ^ 1u);
   const uint64_t limit = p.watchdog_ns;
-  const uint64_t k_blocks = p.k_blocks;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units, p.column_major);
+                                    p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
       sched.init(pair);
       bool ok = true;
+      uint64_t phase = 0;   // k-blocks filled so far: the ring position of the next one
       while (ok && sched.valid()) {
-        const uint64_t w = sched.current_iter;
-        const bool half = sched.part >= 0;          // half unit: the N-half ``part`` alone
+        const bool half = sched.half_unit();          // half unit: the N-half ``part`` alone
         const uint32_t halves = half ? 1u : 2u;
         const int32_t m0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM);
         const int32_t n0 = static_cast<int32_t>(sched.n_idx * kWideBN) + (half ? sched.part * kBN : 0);
         const uint32_t tx_bytes = 2u * (kWideABytes + halves * 2u * kWideBChunkBytes);
-        for (uint32_t k = 0; k < p.k_blocks; ++k) {
-          const uint64_t phase = w * k_blocks + k;
+        for (uint32_t k = sched.k_lo; k < sched.k_hi; ++k, ++phase) {
           const uint32_t s = static_cast<uint32_t>(phase % kWideStages);
           const uint32_t par = static_cast<uint32_t>((phase / kWideStages) & 1u);
           if (!pair_wait_or_abort(bar_consumed + 8u * s, par ^ 1u, abort_flag, peer_abort, limit,
@@ -162,9 +164,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc = idesc_f16(DT, kPairBM, kBN, /*A K-major*/ 0, /*B N-major*/ 1);
       PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                    p.total_units, p.column_major);
+                                    p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
       sched.init(pair);
       bool ok = true;
+      uint64_t phase0 = 0;   // ring position of the current unit's first k-block
       // MMAs of N-half h for the k-block in ring slot s (k: its index within the unit)
       auto issue_half = [&](uint32_t s, uint32_t h, uint32_t k) {
         const uint32_t a_addr = sA0 + s * kWideStageBytes;
@@ -179,13 +182,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       while (ok && sched.valid()) {
         const uint32_t w = sched.current_iter;
-        const uint32_t halves = sched.part >= 0 ? 1u : 2u;
+        const uint32_t halves = sched.half_unit() ? 1u : 2u;
+        const uint32_t nk = sched.k_hi - sched.k_lo;   // k-blocks of this unit (k counts them)
         // N-half 1 of the first ``defer`` k-blocks waits until the epilogue has handed half 1
         // back; those slots are released only once both halves have read them
-        const uint32_t defer =
-            halves == 2u ? (kWideDefer < p.k_blocks ? kWideDefer : p.k_blocks - 1u) : 0u;
-        const uint64_t phase0 = static_cast<uint64_t>(w) * k_blocks;
-        for (uint32_t k = 0; k < p.k_blocks; ++k) {
+        const uint32_t defer = halves == 2u ? (kWideDefer < nk ? kWideDefer : nk - 1u) : 0u;
+        for (uint32_t k = 0; k < nk; ++k) {
           const uint64_t phase = phase0 + k;
           const uint32_t s = static_cast<uint32_t>(phase % kWideStages);
           const uint32_t par = static_cast<uint32_t>((phase / kWideStages) & 1u);
@@ -228,6 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         umma_commit_pair_multicast(bar_tmem_full, 0x3);
+        phase0 += nk;
         sched.next_tile();
       }
       umma_commit_pair_multicast(bar_drain, 0x1);
@@ -239,22 +242,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t q = warp - kFirstEpiWarp;
     const uint32_t sink_even = mapa_shared(smem_u32(&ctl.sink[q]), 0);
     PersistentTileScheduler sched(p.m_blocks, p.n_blocks, p.group, num_pairs, p.split_from,
-                                  p.total_units, p.column_major);
+                                  p.total_units, p.column_major, p.k_blocks, p.sk_tiles);
     sched.init(pair);
     uint32_t chunk = 0;
+    uint32_t sk_bar_uses = 0;   // phases of ctl.sk_bar[q] used so far
     while (sched.valid()) {
       const uint32_t w = sched.current_iter;
       const bool got = pair_wait_or_abort(bar_tmem_full, w & 1u, abort_flag, peer_abort, limit,
                                           kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
-      const bool half = sched.part >= 0;
+      const bool half = sched.half_unit();
       const uint32_t halves = half ? 1u : 2u;
       const int32_t row0 = static_cast<int32_t>(sched.m_idx * kPairBM + rank * kBM + q * 32u);
       const int32_t col0 = static_cast<int32_t>(sched.n_idx) * kWideBN + (half ? sched.part * kBN : 0);
       const uint32_t t_row = tmem_base + ((q * 32u) << 16);
+      // stream-K tail: a contribution goes to this worker's slot (chunk 4h + j for N-half h),
+      // half by half, and is not stored; an owned tile first adds the contributions of workers
+      // sk_lowest_worker .. pair - 1 into its accumulator, half by half, then is stored below
+      const int32_t kind = sched.part;
+      bool sk_ok = true;
+      if (kind == 2) {
 #pragma unroll 1
-      for (uint32_t h = 0; h < 2; ++h) {
+        for (uint32_t h = 0; h < 2; ++h) {
+          sk_write_slot(sk_slot(p.sk_partials, p.sk_slot_f4, pair, rank), t_row + h * kBN,
+                        kBN / kEpiN, h * (kBN / kEpiN), q, lane, sEpi + q * 2u * kEpiBufBytes,
+                        sEpi + (q * 2u + 1u) * kEpiBufBytes);
+          tcgen05_fence_before_sync();
+          pair_report_warp(bar_tmem_empty + 8u * h, rank, lane, sink_even);
+        }
+        sk_publish(p.sk_flags + sk_flag_index(pair, rank, q), p.sk_epoch, lane);
+      } else if (kind == 3) {
+        const uint32_t c_lo = sk_lowest_worker(pair, num_pairs, p.sk_tiles, p.k_blocks,
+                                               sched.sk_tile);
+#pragma unroll 1
+        for (uint32_t h = 0; h < 2 && sk_ok; ++h)
+          sk_ok = sk_gather(p, c_lo, pair, num_pairs, rank, q, lane, t_row + h * kBN, kBN / kEpiN,
+                            h * (kBN / kEpiN), sA0 + q * (kWideStages * kWideStageBytes / kEpiWarps),
+                            smem_u32(&ctl.sk_bar[q]), &sk_bar_uses, h == 0, abort_flag,
+                            peer_abort, limit);
+      }
+      if (!__all_sync(0xffffffffu, sk_ok)) break;
+#pragma unroll 1
+      for (uint32_t h = 0; h < 2 && kind != 2; ++h) {
         if (h >= halves) {
           tcgen05_fence_before_sync();
           pair_report_warp(bar_tmem_empty + 8u * h, rank, lane, sink_even);   // unused half

@@ -22,6 +22,9 @@ struct GemmLaunch {
   uint64_t watchdog_ns;
   int32_t* trace;
   int64_t inject_skip_phase;
+  uint32_t sk_tiles, sk_epoch, sk_slot_f4;   // stream-K tail (0 tiles: none)
+  uint32_t* sk_flags;
+  float4* sk_partials;
 };
 
 // the block-scaled MXFP8 GEMM (one CTA per 128 x 256 tile, the single variant's schedule)

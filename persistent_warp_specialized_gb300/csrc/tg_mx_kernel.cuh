@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
-        const bool half = sched.part >= 0;
+        const bool half = sched.half_unit();
         const int32_t m0 = static_cast<int32_t>(sched.m_idx * kBM);
         const int32_t n0 = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
         const uint32_t sfb_bytes = half ? kMxSfAtomBytes : 2 * kMxSfAtomBytes;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tcgen05_fence_after_sync();
-        const bool half = sched.part >= 0;
+        const bool half = sched.half_unit();
         const uint32_t idesc = half ? idesc_mxf8(kBM, kBN / 2, 0, 0) : idesc_mxf8(kBM, kBN, 0, 0);
         for (uint32_t k = 0; k < p.k_blocks; ++k) {
           const uint64_t phase = static_cast<uint64_t>(w) * k_blocks + k;
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_or_abort(bar_tmem_full, w & 1u, abort_flag, limit, kRoleEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tcgen05_fence_after_sync();
-      const bool half = sched.part >= 0;
+      const bool half = sched.half_unit();
       const int32_t row0 = static_cast<int32_t>(sched.m_idx * kBM + q * 32u);
       const int32_t col0 = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
       const uint32_t t_row = tmem_base + ((q * 32u) << 16);

@@ -166,7 +166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!sf_sched.valid()) return;
         const uint32_t a = static_cast<uint32_t>(sf_phase % kMxPairSfSlots);
         const uint32_t par = static_cast<uint32_t>((sf_phase / kMxPairSfSlots) & 1u);
-        const bool half = sf_sched.part >= 0;
+        const bool half = sf_sched.half_unit();
         const int32_t nu =
             static_cast<int32_t>(sf_sched.n_idx * kBN) + (half ? sf_sched.part * (kBN / 2) : 0);
         const int32_t sfa_row = static_cast<int32_t>(sf_sched.m_idx * 2 + rank);  // A row block
@@ -193,7 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sched.valid()) {
         const uint64_t w = sched.current_iter;
-        const bool half = sched.part >= 0;
+        const bool half = sched.half_unit();
         const int32_t m0 = static_cast<int32_t>(sched.m_idx * (2 * kBM) + rank * kBM);
         const int32_t nu = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
         const int32_t nr = nu + static_cast<int32_t>(rank) * (half ? kBN / 4 : kBN / 2);
@@ -246,7 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tcgen05_fence_after_sync();
-        const uint32_t idesc = sched.part >= 0 ? idesc_mxf8(2 * kBM, kBN / 2, 0, 0)
+        const uint32_t idesc = sched.half_unit() ? idesc_mxf8(2 * kBM, kBN / 2, 0, 0)
                                                : idesc_mxf8(2 * kBM, kBN, 0, 0);
         for (uint32_t j = 0; j < k_stages; ++j) {
           const uint64_t phase = static_cast<uint64_t>(w) * k_stages + j;
@@ -353,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       tcgen05_fence_after_sync();
-      const bool half = sched.part >= 0;
+      const bool half = sched.half_unit();
       const int32_t row0 = static_cast<int32_t>(sched.m_idx * (2 * kBM) + rank * kBM + q * 32u);
       const int32_t col0 = static_cast<int32_t>(sched.n_idx * kBN) + (half ? sched.part * (kBN / 2) : 0);
       uint32_t packed[kBN / kEpiN][kEpiN / 2];

@@ -28,6 +28,8 @@ constexpr uint32_t kWideSmemBytes = kSmemAlignSlack + kWideStages * kWideStageBy
 constexpr uint32_t kWideDefer = TG_WIDE_DEFER;
 static_assert(kWideDefer < kWideStages, "deferred k-blocks hold ring slots");
 static_assert(kWideSmemBytes + 256 <= 232448, "shared memory per CTA (wide pair variant)");
+static_assert(kWideStages * kWideStageBytes / kEpiWarps >= (kBN / kEpiN) * 8192,
+              "a stream-K owner stages one N-half of a contribution per warp in the ring");
 static_assert(kWideBK == kKAtom, "a wide stage holds one 128-byte swizzle atom of A");
 static_assert(2 * kBN <= (int)kTmemCols, "the wide accumulator spans both TMEM halves");
 

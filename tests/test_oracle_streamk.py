@@ -69,13 +69,3 @@ def test_worked_partition_4096_cube_pair_tiles():
     assert s.streamk_segments(2, 76, 28, 32) == [(1, 0, 3, False), (0, 23, 32, True)]
     assert s.streamk_contributors(0, 76, 28, 32) == (2, [0, 1])
     assert s.streamk_range(75, 76, 28, 32)[1] == 896
-
-
-def test_rule():
-    assert s.streamk_applies(256, 76, 32)          # 4096^3, 256 x 256 tiles: 28 tail tiles
-    assert s.streamk_applies(512, 76, 128)         # 8192^3, 256 x 512 tiles: 56
-    assert not s.streamk_applies(448, 76, 16)      # 4000 x 7000 x 2048: 68 of 76, a near-full wave
-    assert s.streamk_applies(1024, 76, 64)         # 8192^3, 256 x 256 tiles: 36
-    assert not s.streamk_applies(76 * 3, 76, 64)   # no partial wave
-    assert not s.streamk_applies(76 + 10, 76, 64)  # 10 < 76/4
-    assert not s.streamk_applies(76 + 30, 76, 4)   # 30 x 4 < 8 x 76 k-blocks
