@@ -117,7 +117,7 @@ int tg_gemm_persistent(const void* A_dev, const void* B_dev, void* C_dev,
  * variant ceil(M/256) x ceil(N/512) tiles (its tail-split half units are 256 x 256).
  * TG_VARIANT_AUTO takes the wide pair variant when its tiles fill at least one wave of resident
  * pairs and K >= 6144, or four waves and K >= 4096; else the pair variant when its tiles fill at
- * least one wave; else the single one.  Unless the variant carries TG_SCHEDULE_PLAIN,
+ * least one wave, or when K >= 4096 and M >= 256; else the single one.  Unless the variant carries TG_SCHEDULE_PLAIN,
  * TG_SCHEDULE_COLUMN_MAJOR or TG_SCHEDULE_GROUP, AUTO also picks the traversal: whole rows of
  * tiles when all of B fits in 64 MiB (half of the L2), whole columns when only A does, else
  * groups of 8 in row order, or for the wide pair variant groups of round(sqrt(2 x workers))
