@@ -330,8 +330,9 @@ int tg_mxfp8_pack_scales(const void* sf_dev, void* packed_dev, int64_t rows, int
  *   C must not overlap any input.  M == 0 or N == 0: nothing is done.  K == 0: C is
  *   zero-filled.
  * Kernels: one CTA per 128 x 256 output tile (TG_VARIANT_SINGLE), or a CTA pair per 256 x 256
- * tile (TG_VARIANT_PAIR, tcgen05 cta_group::2); tg_gemm_mxfp8 chooses as TG_VARIANT_AUTO does
- * for tg_gemm_persistent, and tg_gemm_launch_shape gives the launch of either.  Persistent,
+ * tile (TG_VARIANT_PAIR, tcgen05 cta_group::2); tg_gemm_mxfp8 (TG_VARIANT_AUTO) takes the pair
+ * kernel when its tiles fill at least one wave of resident pairs, or when K >= 4096 and
+ * M >= 256, else the single one, and tg_gemm_launch_shape gives the launch of either.  Persistent,
  * grouped order with the tail split.  Asynchronous; errors as for tg_gemm_persistent.
  * Inputs that hold NaN patterns give unspecified outputs.
  */

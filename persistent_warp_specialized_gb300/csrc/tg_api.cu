@@ -183,12 +183,23 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
   return TG_OK;
 }
 
-// The variant TG_VARIANT_AUTO resolves to: the CTA-pair kernel once its 256 x 256 tiles fill
-// at least one wave of resident pairs (measured faster there at every workload size), else
-// the single-CTA kernel, whose smaller tiles spread a small problem over more SMs.
-int auto_variant(int64_t M, int64_t N, int64_t /*K*/, int max_pairs) {
+// The variant TG_VARIANT_AUTO resolves to (both GEMMs): the CTA-pair kernel once its 256 x 256
+// tiles fill at least one wave of resident pairs (measured faster there at every workload
+// size), or below a wave once K >= 4096 and M fills the pair's 256 rows; else the single-CTA
+// kernel, whose smaller tiles spread a short-K problem over more SMs.  Below a wave, a 256 x 256
+// pair MMA reads fewer shared-memory bytes per flop than the single CTA's 128 x 256 one, which
+// pays once K is long enough to amortise the pair's pipeline fill.  Same box, L2 flushed before
+// each of 50 launches, medians (single / pair TFLOP/s): dense bf16 1024 x 1024 x 4096 323 / 350,
+// x 8192 365 / 419, 512 x 512 x 8192 94 / 110, 1536 x 1536 x 4096 675 / 755, 2048 x 2048 x 4096
+// 1119 / 1117; MXFP8 1024 x 1024 x 8192 524 / 599, 512 x 512 x 8192 131 / 150, 2048 x 2048 x
+// 4096 1523 / 1525 (back to back, 1890 / 2007).  With K <= 2048 the single kernel is as fast or
+// faster (dense 1024^3 175 / 150, 2048^3 839 / 838; MXFP8 1024 x 1024 x 2048 back to back 435 /
+// 404).
+int auto_variant(int64_t M, int64_t N, int64_t K, int max_pairs) {
   const int64_t pair_tiles = ((M + tg::kPairBM - 1) / tg::kPairBM) * ((N + tg::kBN - 1) / tg::kBN);
-  return (max_pairs > 0 && pair_tiles >= max_pairs) ? TG_VARIANT_PAIR : TG_VARIANT_SINGLE;
+  if (max_pairs < 1) return TG_VARIANT_SINGLE;
+  return (pair_tiles >= max_pairs || (K >= 4096 && M >= tg::kPairBM)) ? TG_VARIANT_PAIR
+                                                                      : TG_VARIANT_SINGLE;
 }
 
 // The dense GEMM's choice: the wide pair kernel (256 x 512 tiles) when its tiles fill at least
@@ -199,21 +210,12 @@ int auto_variant(int64_t M, int64_t N, int64_t /*K*/, int max_pairs) {
 // 8192^3 +2.6 %); K = 4096 ties (8192 x 8192 1904 / 1894, 12288 x 12288 1937 / 1939, 6144 x 6144
 // 1858 / 1862), so wide is kept there only for four waves or more; K = 2048 favours the pair
 // kernel (8192 x 8192 1858 / 1773).
-// Below a wave of pair tiles the pair kernel still wins once K >= 4096 and M fills its 256 rows:
-// a 256 x 256 pair MMA reads fewer shared-memory bytes per flop than the single CTA's 128 x 256
-// one, which matters once K is long enough to amortise the pair's deeper pipeline fill.  Same
-// box, L2 flushed before each of 50 launches, medians (single / pair TFLOP/s): 1024 x 1024 x 4096
-// 323 / 350, x 8192 365 / 419, 512 x 512 x 8192 94 / 110, 1536 x 1536 x 4096 675 / 755,
-// 1024 x 2048 x 8192 729 / 798, 2048 x 2048 x 8192 1290 / 1341, 2048 x 2048 x 4096 1119 / 1117;
-// at K <= 2048 the single kernel is as fast or faster (1024^3 175 / 150, 2048^3 839 / 838,
-// 1024 x 1024 x 2048 233 / 233).
 int auto_variant_dense(int64_t M, int64_t N, int64_t K, int max_pairs) {
   const int64_t wide_tiles =
       ((M + tg::kPairBM - 1) / tg::kPairBM) * ((N + tg::kWideBN - 1) / tg::kWideBN);
   if (max_pairs > 0 && ((K >= 6144 && wide_tiles >= max_pairs) ||
                         (K >= 4096 && wide_tiles >= 4 * int64_t(max_pairs))))
     return TG_VARIANT_PAIR_WIDE;
-  if (max_pairs > 0 && K >= 4096 && M >= tg::kPairBM) return TG_VARIANT_PAIR;
   return auto_variant(M, N, K, max_pairs);
 }
 

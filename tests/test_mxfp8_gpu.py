@@ -223,3 +223,13 @@ def test_mxfp8_gemm_convenience_matches_the_oracle():
     torch.cuda.synchronize()
     assert c.shape == (M, N) and c.dtype == torch.bfloat16
     assert np.array_equal(wl.bits(c.cpu()), ref_bits(a, sa, b, sb))
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 512, 8192), (256, 1024, 4096)])
+def test_auto_long_k_below_a_wave(M, N, K):
+    # tg_gemm_mxfp8 takes the CTA-pair kernel here (fewer pair tiles than a wave, K >= 4096):
+    # the same gate and bound as every other MXFP8 parity case
+    assert tg.tg_gemm_launch_shape(M, N, K, mxfp8=True)["variant"] == tg.TG_VARIANT_PAIR
+    a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed=M + K)
+    check_tolerance(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb), a, sa, b, sb, "bf16",
+                    "auto long K")

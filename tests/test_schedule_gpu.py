@@ -245,12 +245,13 @@ def test_auto_traversal_is_reported_and_followed(M, N, K, rows):
                                         (128, 1024, 8192, 1), (2048, 1024, 4096, 2)])
 def test_auto_takes_the_pair_kernel_for_long_k_below_a_wave(M, N, K, want):
     # below one wave of pair tiles, TG_VARIANT_AUTO still takes the CTA-pair kernel once
-    # K >= 4096 and M fills its 256 rows (measured faster there), else the single-CTA kernel;
-    # the product is exact on integer inputs either way
+    # K >= 4096 and M fills its 256 rows (measured faster there), else the single-CTA kernel,
+    # for the dense and the MXFP8 GEMM alike; the product is exact on integer inputs either way
     shape = tg.tg_gemm_launch_shape(M, N, K)
     pair_tiles = ((M + 255) // 256) * ((N + 255) // 256)
     assert pair_tiles < torch.cuda.get_device_properties(0).multi_processor_count // 2
     assert shape["variant"] == want
+    assert tg.tg_gemm_launch_shape(M, N, K, mxfp8=True)["variant"] == want
     a, b = wl.small_int_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=K + M)
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     tg.tg_gemm_persistent(a.cuda(), b.cuda(), c, M, N, K, "bf16")
