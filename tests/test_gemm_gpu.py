@@ -204,3 +204,68 @@ def test_direct_store_epilogue_fp16_within_tolerance(variant):
     tg.tg_gemm_persistent_ex(a.cuda(), b.cuda(), c, M, N, K, "f16", variant=variant, direct=True)
     torch.cuda.synchronize()
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "f16"), "f16", "direct epilogue")
+
+
+def _two_term(pairs, dtype, M=256, N=512, K=64):
+    """A, B with C[i, j] = x_i + y_i / 2 for (x_i, y_i) = pairs[i % len(pairs)]: A holds x in
+    column 0 and y in column 1, B holds ones in row 0 and halves in row 1, zeros elsewhere.
+    Every product and the one non-trivial sum are exact in fp32, so the kernel's output must
+    be the oracle's rounding of the exact sum, bit for bit."""
+    tdt = wl.TORCH_DTYPES[dtype]
+    a = torch.zeros((M, K), dtype=torch.float64)
+    for i in range(M):
+        a[i, 0], a[i, 1] = pairs[i % len(pairs)]
+    b = torch.zeros((K, N), dtype=torch.float64)
+    b[0, :] = 1.0
+    b[1, :] = 0.5
+    a16, b16 = a.to(tdt), b.to(tdt)
+    assert torch.equal(a16.double(), a) and torch.equal(b16.double(), b), "inputs must be exact"
+    return a16.contiguous(), b16.contiguous()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fp16_outputs_overflow_to_inf_as_rne_does(variant):
+    # 65504 is the largest finite fp16; sums below the midpoint 65520 stay 65504, the midpoint
+    # itself ties to even (the infinity), beyond it is inf, and the same on the negative side
+    big = 65504.0
+    pairs = [(big, 0.0), (big, 16.0), (big, 30.0), (big, 32.0), (big, 64.0), (big, big),
+             (32768.0, big), (-big, -30.0), (-big, -32.0), (-big, -big), (60000.0, 10000.0),
+             (1.0, 2.0)]
+    a, b = _two_term(pairs, "f16")
+    got = run_gpu(a, b, "f16", variant=variant)
+    want = oracle_bits(a, b, "f16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "f16")
+    assert np.isposinf(vals).any() and np.isneginf(vals).any() and (vals == big).any()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fp16_subnormal_outputs_round_to_nearest_even(variant):
+    # u = 2^-24 is the least fp16 subnormal; x + y/2 with y = u puts the exact sum half an ulp
+    # between two subnormals: 0.5 u -> 0, 1.5 u -> 2u, 2.5 u -> 2u, 3.5 u -> 4u (ties to even)
+    u = 2.0 ** -24
+    pairs = [(0.0, u), (u, u), (2 * u, u), (3 * u, u), (2.0 ** -14, -u), (-u, -u), (1000 * u, u),
+             (2.0 ** -15, 2 * u),
+             # normal inputs whose sum cancels into the subnormal range: 2^-13 - (2^-13 - u) = u
+             (2.0 ** -13, -(2.0 ** -12 - 2.0 ** -23))]
+    a, b = _two_term(pairs, "f16")
+    got = run_gpu(a, b, "f16", variant=variant)
+    want = oracle_bits(a, b, "f16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "f16")
+    assert ((vals != 0) & (np.abs(vals) < 2.0 ** -14)).any()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_bf16_outputs_at_the_top_of_the_range(variant):
+    # the largest finite bf16 is (2 - 2^-7) 2^127; sums that stay below the rounding midpoint to
+    # 2^128 keep it, sums beyond the fp32 range are inf in the accumulator and in the oracle
+    top = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    pairs = [(2.0 ** 127, 2.0 ** 127), (top, 0.0), (top, top * 2.0 ** -8), (top, top),
+             (-top, -top), (2.0 ** 126, 2.0 ** 127), (1.0, 2.0)]
+    a, b = _two_term(pairs, "bf16")
+    got = run_gpu(a, b, "bf16", variant=variant)
+    want = oracle_bits(a, b, "bf16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "bf16")
+    assert np.isposinf(vals).any() and np.isneginf(vals).any() and (vals == top).any()
