@@ -233,3 +233,58 @@ def test_auto_long_k_below_a_wave(M, N, K):
     a, sa, b, sb = wl.make_mx_inputs(M, N, K, seed=M + K)
     check_tolerance(run_mx(a, sa, b, sb), ref_bits(a, sa, b, sb), a, sa, b, sb, "bf16",
                     "auto long K")
+
+
+def _block_terms(rows, out_rows=256, N=256, K=128):
+    """A, SFA, B, SFB with C[i, j] = sum_t x_t 2^(e_t) over the terms (x_t, e_t) of
+    rows[i % len(rows)] (at most K / 32 terms, one per 32-element block): A holds x_t at the first
+    element of block t with scale 2^(e_t); B holds 1.0 there with scale 1.  Every partial sum in
+    the cases below is exact in fp32, in any order."""
+    a = torch.zeros((out_rows, K), dtype=torch.float32)
+    sa = torch.full((out_rows, K // 32), 127, dtype=torch.uint8)
+    for i in range(out_rows):
+        for t, (x, e) in enumerate(rows[i % len(rows)]):
+            a[i, 32 * t] = x
+            sa[i, t] = 127 + e
+    b = torch.zeros((N, K), dtype=torch.float32)
+    b[:, 0::32] = 1.0
+    sb = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    a8 = a.to(torch.float8_e4m3fn)
+    assert torch.equal(a8.float(), a), "elements must be exact in E4M3"
+    return (a8.view(torch.uint8).contiguous(), sa, b.to(torch.float8_e4m3fn).view(torch.uint8)
+            .contiguous(), sb)
+
+
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_output_rounding_at_the_edges_of_fp16_and_bf16(variant):
+    u = -24                                   # 2^-24: the least fp16 subnormal
+    f16_rows = [
+        [(448.0, 7)],                         # 57344: finite
+        [(448.0, 7), (1.0, 13), (-1.0, 4)],   # 65520: the midpoint above 65504, ties to inf
+        [(448.0, 7), (1.0, 13)],              # 65536: inf
+        [(-448.0, 7), (-1.0, 13), (1.0, 4)],  # -65520: -inf
+        [(448.0, 7), (1.75, 12), (-1.0, 4)],  # 64496: halfway to 64512, ties to it (finite)
+        [(1.5, u)],                           # 1.5 u: ties to 2u
+        [(0.5, u)],                           # 0.5 u: ties to 0
+        [(1.0, u), (1.0, u - 2)],             # 1.25 u: u
+        [(1.0, -14), (-1.0, u)],              # 2^-14 - u: the largest subnormal
+    ]
+    a, sa, b, sb = _block_terms(f16_rows)
+    got = run_mx(a, sa, b, sb, "f16", variant=variant)
+    want = ref_bits(a, sa, b, sb, "f16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "f16")
+    assert np.isposinf(vals).any() and np.isneginf(vals).any()
+    assert ((vals != 0) & (np.abs(vals) < 2.0 ** -14)).any()
+    bf16_rows = [
+        [(448.0, 120)],                       # 5.96e38: past the fp32 range, inf
+        [(-448.0, 120)],                      # -inf
+        [(1.0, 127), (1.0, 126)],             # 1.5 x 2^127: finite, exact
+        [(1.75, 127)],                        # 2.98e38: finite
+    ]
+    a, sa, b, sb = _block_terms(bf16_rows)
+    got = run_mx(a, sa, b, sb, "bf16", variant=variant)
+    want = ref_bits(a, sa, b, sb, "bf16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "bf16")
+    assert np.isposinf(vals).any() and np.isneginf(vals).any() and np.isfinite(vals).any()
