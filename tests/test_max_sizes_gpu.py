@@ -1,0 +1,115 @@
+"""GPU: the dense GEMM at the largest M and N the C ABI accepts (M, N < 2^31).
+
+A problem with M = 2^31 - 1 (or N = 2^31 - 8, the largest multiple of 8) and the other two
+extents 8 holds 32 GiB in each of its long operand and C.  The long operand is written on the
+device in chunks by plain torch arithmetic from an integer formula, and the oracle rebuilds the
+rows (or columns) it checks from the same formula on the host, so no input or expected value
+comes from the kernels.  Integer entries keep every sum exact in fp32: the sampled outputs must
+equal the oracle bit for bit, among them the last row (column) and the rows around tile edges
+near 2^31.  Skipped when the device lacks the memory.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import persistent_warp_specialized_gb300 as tg
+from persistent_warp_specialized_gb300 import workloads as wl
+from oracle import gemm as ogemm
+
+from gpu_helpers import VARIANTS, ensure_library
+
+pytestmark = pytest.mark.gpu
+
+BIG = 2 ** 31 - 1
+CHUNK = 1 << 26
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def need_gib(n):
+    free, _ = torch.cuda.mem_get_info()
+    if free < n * (1 << 30):
+        pytest.skip(f"needs {n} GiB of free device memory, {free >> 30} GiB free")
+
+
+def formula(i, k, a, b, mod):
+    """((i * a + k * b) mod mod) - mod // 2, elementwise on int64 arrays or tensors."""
+    return (i * a + k * b) % mod - mod // 2
+
+
+def fill_long(t, along_rows, a, b, mod):
+    """t[i, k] (along_rows) or t[k, j] = formula(index along the long side, short index)."""
+    long_n = t.shape[0] if along_rows else t.shape[1]
+    short = torch.arange(t.shape[1] if along_rows else t.shape[0], device=t.device,
+                         dtype=torch.int64)
+    for s in range(0, long_n, CHUNK):
+        e = min(long_n, s + CHUNK)
+        idx = torch.arange(s, e, device=t.device, dtype=torch.int64)
+        if along_rows:
+            t[s:e] = formula(idx[:, None], short[None, :], a, b, mod).to(t.dtype)
+        else:
+            t[:, s:e] = formula(idx[None, :], short[:, None], a, b, mod).to(t.dtype)
+
+
+def sample_indices(n, tile):
+    """First, last and tile-edge indices near the end of a long extent of n, plus a few more."""
+    picks = {0, 1, n - 1, n - 2, n // 2}
+    last_tile = (n - 1) // tile * tile
+    picks.update({last_tile, last_tile - 1, last_tile + 127, last_tile - tile})
+    gen = np.random.default_rng(n)
+    picks.update(int(x) for x in gen.integers(0, n, 8))
+    return sorted(p for p in picks if 0 <= p < n)
+
+
+@pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
+def test_largest_m(variant):
+    need_gib(80)
+    M, N, K = BIG, 8, 8
+    dt = torch.bfloat16
+    a = torch.empty((M, K), dtype=dt, device="cuda")
+    fill_long(a, True, 37, 11, 7)
+    b_cpu = wl.small_int_inputs(8, N, K, "bf16", lo=-2, hi=2, seed=5)[1]
+    b = b_cpu.cuda()
+    c = torch.empty((M, N), dtype=dt, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_persistent_ex(a, b, c, M, N, K, "bf16", variant=variant)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    rows = sample_indices(M, 256)
+    got = wl.bits(c[rows].cpu())
+    a_rows = torch.from_numpy(formula(np.array(rows, dtype=np.int64)[:, None],
+                                      np.arange(K, dtype=np.int64)[None, :], 37, 11, 7)
+                              .astype(np.float64)).to(dt)
+    want = ogemm.gemm_ref(wl.bits(a_rows), wl.bits(b_cpu), "bf16")
+    assert np.array_equal(got, want), rows
+    del a, c
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
+def test_largest_n(variant):
+    need_gib(80)
+    M, N, K = 8, BIG - 7, 8          # 2^31 - 8: the largest multiple of 8 below 2^31
+    dt = torch.bfloat16
+    b = torch.empty((K, N), dtype=dt, device="cuda")
+    fill_long(b, False, 13, 5, 9)
+    a_cpu = wl.small_int_inputs(M, 8, K, "bf16", lo=-2, hi=2, seed=6)[0]
+    a = a_cpu.cuda()
+    c = torch.empty((M, N), dtype=dt, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_persistent_ex(a, b, c, M, N, K, "bf16", variant=variant)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    cols = sample_indices(N, 512)
+    got = wl.bits(c[:, cols].cpu())
+    b_cols = torch.from_numpy(formula(np.array(cols, dtype=np.int64)[None, :],
+                                      np.arange(K, dtype=np.int64)[:, None], 13, 5, 9)
+                              .astype(np.float64)).to(dt)
+    want = ogemm.gemm_ref(wl.bits(a_cpu), wl.bits(b_cols.contiguous()), "bf16")
+    assert np.array_equal(got, want), cols
+    del b, c
+    torch.cuda.empty_cache()
