@@ -256,7 +256,9 @@ int tg_gemm_launch_shape(int64_t M, int64_t N, int64_t K, int variant, int* vari
  *     *units); row u (the unit id) receives (worker, w, bx, by, part) as the epilogue that
  *     stored unit u saw them (worker = CTA, or CTA pair) -- evidence that the kernel followed
  *     the schedule of tg_tile_schedule_ex.
- *   watchdog_ns: limit for every wait inside the kernel (0 = the default of about 4 s).
+ *   watchdog_ns: limit for every wait inside the kernel (0 = the default, which every other
+ *     entry point uses: 2^32 ns, about 4.3 s, plus 2 us per k-block of K, so that a wait that
+ *     spans one tile's whole K is not cut short).
  *   inject_skip_phase: -1 for none; otherwise cta * 2^32 + phase: the producer of CTA ``cta``
  *     (0 when inject_skip_phase < 2^32) never arms or fills that pipeline phase, so the MMA
  *     role's wait on it cannot complete: the watchdog must fire, every role must stop, and the

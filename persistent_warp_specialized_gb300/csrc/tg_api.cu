@@ -183,6 +183,15 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
   return TG_OK;
 }
 
+// The default limit of every bounded wait in the kernels when the caller gives none: the
+// fixed kDefaultWatchdogNs plus 2 us per k-block of K.  The longest legitimate wait spans one
+// unit's whole K (the epilogue waiting for its accumulator), and a k-block takes at most about
+// 0.5 us on GB300 even on a CTA pair's half-width unit, so with K near 2^31 (2^25 k-blocks of
+// 64, ~12 s per unit, measured) a fixed limit of ~4 s stopped a correct GEMM.
+uint64_t default_watchdog_ns(uint32_t k_blocks) {
+  return tg::kDefaultWatchdogNs + uint64_t(k_blocks) * 2000u;
+}
+
 // The variant TG_VARIANT_AUTO resolves to (both GEMMs): the CTA-pair kernel once its 256 x 256
 // tiles fill at least one wave of resident pairs (measured faster there at every workload
 // size), or below a wave once K >= 4096 and M fills the pair's 256 rows; else the single-CTA
@@ -413,7 +422,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   l.k_blocks = static_cast<uint32_t>((K + block_k - 1) / block_k);
   l.group = group;
   l.grid = sh.ctas;
-  l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
+  l.watchdog_ns = watchdog_ns ? watchdog_ns : default_watchdog_ns(l.k_blocks);
   l.trace = trace;
   l.inject_skip_phase = inject;
   l.sk_tiles = sh.sk_tiles;
@@ -549,7 +558,7 @@ int mx_impl(const void* A, const void* SFA, const void* B, const void* SFB, void
   l.total_units = sh.units;
   l.column_major = (flags & TG_SCHEDULE_COLUMN_MAJOR) ? 1u : 0u;
   l.grid = sh.ctas;
-  l.watchdog_ns = watchdog_ns ? watchdog_ns : tg::kDefaultWatchdogNs;
+  l.watchdog_ns = watchdog_ns ? watchdog_ns : default_watchdog_ns(l.k_blocks);
   l.trace = trace;
   l.inject_skip_phase = inject;
   cudaError_t e;

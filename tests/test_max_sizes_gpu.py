@@ -113,3 +113,31 @@ def test_largest_n(variant):
     assert np.array_equal(got, want), cols
     del b, c
     torch.cuda.empty_cache()
+
+
+def test_largest_k():
+    # K = 2^31 - 8 with M = N = 8: one tile walks 2^25 k-blocks, the last one partial.  A and B
+    # are zero except at a few k spread over the range (both sides of the last k-block's start
+    # among them), so C is their exact sum: a k-block skipped, repeated or loaded at a wrong
+    # coordinate changes it.
+    need_gib(80)
+    M, N, K = 8, 8, BIG - 7
+    dt = torch.bfloat16
+    ks = [0, 63, 64, 1 << 30, K - 72, K - 64 - 1, K - 57, K - 9, K - 1]
+    gen = torch.Generator().manual_seed(9)
+    a_cols = torch.randint(-3, 4, (M, len(ks)), generator=gen).to(dt)
+    b_rows = torch.randint(-3, 4, (len(ks), N), generator=gen).to(dt)
+    a = torch.zeros((M, K), dtype=dt, device="cuda")
+    b = torch.zeros((K, N), dtype=dt, device="cuda")
+    idx = torch.tensor(ks, dtype=torch.int64, device="cuda")
+    a[:, idx] = a_cols.cuda()
+    b[idx, :] = b_rows.cuda()
+    c = torch.empty((M, N), dtype=dt, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_persistent(a, b, c, M, N, K, "bf16")
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    want = ogemm.gemm_ref(wl.bits(a_cols), wl.bits(b_rows), "bf16")
+    assert np.array_equal(wl.bits(c.cpu()), want)
+    del a, b, c
+    torch.cuda.empty_cache()
