@@ -242,7 +242,8 @@ cudaError_t launch_mxfp8(int out_dtype, bool debug, int variant, const MxLaunch&
 cudaError_t launch_mx_pack(const void* sf, void* out, uint32_t rows, uint32_t k_blocks,
                            uint32_t row_blocks, cudaStream_t stream) {
   if (k_blocks == 0 || row_blocks == 0) return cudaSuccess;
-  const dim3 grid(row_blocks, (k_blocks + kMxPackKb - 1) / kMxPackKb);
+  const uint32_t groups = (k_blocks + kMxPackKb - 1) / kMxPackKb;
+  const dim3 grid(row_blocks, groups < 65535u ? groups : 65535u);   // the kernel strides over y
   return launch_pdl(mx_pack_scales_kernel, grid, kMxPackThreads, 0, stream,
                     static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, k_blocks,
                     row_blocks);

@@ -15,7 +15,7 @@ import torch
 
 import persistent_warp_specialized_gb300 as tg
 from persistent_warp_specialized_gb300 import workloads as wl
-from oracle import gemm as ogemm
+from oracle import gemm as ogemm, mx
 
 from gpu_helpers import VARIANTS, ensure_library
 
@@ -140,4 +140,59 @@ def test_largest_k():
     want = ogemm.gemm_ref(wl.bits(a_cols), wl.bits(b_rows), "bf16")
     assert np.array_equal(wl.bits(c.cpu()), want)
     del a, b, c
+    torch.cuda.empty_cache()
+
+
+def test_mxfp8_beyond_one_pass_of_the_pack_grid():
+    # 524297 k-blocks of 128: 65538 groups of 8, more than the 65535 a grid's y extent holds, so
+    # the scale pack strides over them.  Sampled atoms (the last among them) against the
+    # documented layout, then the GEMM at that K: A and B are zero except at a few k, one per
+    # 32-element block and spread over the range, so C is their exact scaled sum, which the
+    # oracle computes on the same entries with the same block scales gathered into a short K.
+    need_gib(8)
+    M = N = 8
+    kb = 8 * 65535 + 17
+    K = 128 * kb
+    gen = torch.Generator().manual_seed(12)
+    # scales 2^-3 .. 2^3: the six terms of a sum stay within 18 bits, exact in fp32
+    sfa = torch.randint(124, 131, (M, K // 32), generator=gen).to(torch.uint8)
+    sfb = torch.randint(124, 131, (N, K // 32), generator=gen).to(torch.uint8)
+    pa = tg.mxfp8_pack(sfa.cuda(), K)
+    pb = tg.mxfp8_pack(sfb.cuda(), K)
+    torch.cuda.synchronize()
+    row_blocks = 2                               # 8 rows pad to 256: two blocks of 128
+    for k in [0, 7, 8, 65535 * 8 - 1, 65535 * 8, kb - 1]:
+        for b in range(row_blocks):
+            atom = pa[(k * row_blocks + b) * 512:(k * row_blocks + b + 1) * 512].cpu().numpy()
+            want = np.zeros(512, np.uint8)
+            for r in range(128):
+                if b * 128 + r < M:
+                    off = (r % 32) * 16 + (r // 32) * 4
+                    want[off:off + 4] = sfa[b * 128 + r, 4 * k:4 * k + 4].numpy()
+            assert np.array_equal(atom, want), (k, b)
+    ks = [5, 32 * 1000 + 3, K // 2 + 7, 128 * (65535 * 8) - 32 + 1, K - 33, K - 1]
+    e4m3 = lambda v: v.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+    a_vals = torch.randint(-3, 4, (M, len(ks)), generator=gen).float()
+    b_vals = torch.randint(-3, 4, (N, len(ks)), generator=gen).float()
+    a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    b = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    idx = torch.tensor(ks, dtype=torch.int64, device="cuda")
+    a[:, idx] = e4m3(a_vals).cuda()
+    b[:, idx] = e4m3(b_vals).cuda()
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    c.view(torch.int16).fill_(-1)
+    tg.tg_gemm_mxfp8(a, pa, b, pb, c, M, N, K, "bf16")
+    torch.cuda.synchronize()
+    assert tg.tg_device_status() == 0
+    # the same entries in a K of 32 per position, each block with its original scale
+    blocks = [k // 32 for k in ks]
+    assert len(set(blocks)) == len(blocks)
+    a_c = torch.zeros((M, 32 * len(ks)), dtype=torch.uint8)
+    b_c = torch.zeros((N, 32 * len(ks)), dtype=torch.uint8)
+    a_c[:, 32 * torch.arange(len(ks)) + torch.tensor([k % 32 for k in ks])] = e4m3(a_vals)
+    b_c[:, 32 * torch.arange(len(ks)) + torch.tensor([k % 32 for k in ks])] = e4m3(b_vals)
+    want = mx.gemm_mxfp8_ref(a_c.numpy(), sfa[:, blocks].numpy(), b_c.numpy(),
+                             sfb[:, blocks].numpy(), "bf16")
+    assert np.array_equal(wl.bits(c.cpu()), want)
+    del a, b, c, pa, pb
     torch.cuda.empty_cache()
