@@ -206,9 +206,9 @@ def test_direct_store_epilogue_fp16_within_tolerance(variant):
     assert_within_tolerance(wl.bits(c.cpu()), oracle_bits(a, b, "f16"), "f16", "direct epilogue")
 
 
-def _two_term(pairs, dtype, M=256, N=512, K=64):
-    """A, B with C[i, j] = x_i + y_i / 2 for (x_i, y_i) = pairs[i % len(pairs)]: A holds x in
-    column 0 and y in column 1, B holds ones in row 0 and halves in row 1, zeros elsewhere.
+def _two_term(pairs, dtype, M=256, N=512, K=64, w=0.5):
+    """A, B with C[i, j] = x_i + w y_i for (x_i, y_i) = pairs[i % len(pairs)]: A holds x in
+    column 0 and y in column 1, B holds ones in row 0 and w in row 1, zeros elsewhere.
     Every product and the one non-trivial sum are exact in fp32, so the kernel's output must
     be the oracle's rounding of the exact sum, bit for bit."""
     tdt = wl.TORCH_DTYPES[dtype]
@@ -217,7 +217,7 @@ def _two_term(pairs, dtype, M=256, N=512, K=64):
         a[i, 0], a[i, 1] = pairs[i % len(pairs)]
     b = torch.zeros((K, N), dtype=torch.float64)
     b[0, :] = 1.0
-    b[1, :] = 0.5
+    b[1, :] = w
     a16, b16 = a.to(tdt), b.to(tdt)
     assert torch.equal(a16.double(), a) and torch.equal(b16.double(), b), "inputs must be exact"
     return a16.contiguous(), b16.contiguous()
@@ -269,3 +269,22 @@ def test_bf16_outputs_at_the_top_of_the_range(variant):
     assert np.array_equal(got, want)
     vals = formats.decode(want, "bf16")
     assert np.isposinf(vals).any() and np.isneginf(vals).any() and (vals == top).any()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_bf16_subnormals_are_kept(variant):
+    # bf16 has fp32's exponent range, so its subnormals (multiples of s = 2^-133) are fp32
+    # subnormals too: the tensor core keeps them (no flush to zero) in the inputs, in products
+    # and in the fp32 sum, and the output rounds to nearest even among them
+    s = 2.0 ** -133
+    w = 2.0 ** -60
+    pairs = [(2.0 ** -127, 0.0), (s, 0.0), (0.0, 2.0 ** -70),          # copies and a product
+             (2.0 ** -127, 2.0 ** -70), (64 * s, 2.0 ** -74),            # 72 s; 64.5 s -> 64 s
+             (65 * s, 2.0 ** -74), (-3 * s, -(2.0 ** -74)),                # 66 s; -4 s
+             (2.0 ** -126, -(2.0 ** -67))]                              # normal - half: 64 s
+    a, b = _two_term(pairs, "bf16", w=w)
+    got = run_gpu(a, b, "bf16", variant=variant)
+    want = oracle_bits(a, b, "bf16")
+    assert np.array_equal(got, want)
+    vals = formats.decode(want, "bf16")
+    assert ((vals != 0) & (np.abs(vals) < 2.0 ** -126)).sum() > vals.size // 2
